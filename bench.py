@@ -1,0 +1,404 @@
+"""Benchmark: scoring one prefetched subtree batch (and walking it) on GB300.
+
+One step = the whole hot path over one subtree batch already resident in HBM:
+per-token log p0 / log q_tau of every row (ps_score_rows), suffix sums and
+log A per request (ps_assemble_subtree), and the walk (ps_walk_subtree).
+
+Default workload: Qwen3-like vocabulary V = 151936 bf16, T = 1024,
+N_pf = 16 BFS, alpha = 4, tau = 0.25 (about 13.7k rows, 4.2 GB of logits,
+far larger than the 129 MB L2, so no flush is needed between steps).
+
+metric  scored suffix tokens per second (sum over requests of T - c_i,
+        whole job over all ranks); logits GB/s and the HBM roofline of the
+        scoring kernel are reported alongside.
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank scores its own batch (independent problems, weak
+scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scored suffix tokens/sec and logits GB/s vs GB300 HBM peak per subtree batch"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
+FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
+# DRAM bytes per launch of the scoring kernel on the default workload, from one
+# ncu capture (profiles/score_rows_config2_ncu.md), valid for this source hash.
+NCU_TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha1() -> str:
+    h = hashlib.sha1()
+    for name in ("ps_score_rows.cu", "ps_internal.cuh"):
+        with open(os.path.join(ROOT, "mh_prefetch_subtree_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if self.t0 is not None and self.t0 <= t <= self.t1]
+        use = inside if inside else [r for _, r in self.rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        mx = [num(r[2]) for r in use if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in use for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_region": len(inside),
+                "power_w_max": max((num(r[3]) or 0.0) for r in use)}
+
+
+def build_workload(config: int, dev, rank: int):
+    from synth import make_workload
+    kw = {}
+    if rank:
+        kw["seed"] = 10086 + config + 7919 * rank
+    return make_workload(config, device=dev, **kw)
+
+
+def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the same batch."""
+    import oracle
+    from tests.gpu_harness import oracle_rows   # block-wise host copies for the oracle
+    threads = oracle.default_threads()
+    lay = w.layout
+    # sample: the root and the first requests whose rows fit ~max_seconds
+    # of oracle work at ~0.5 G logits/s per 8 cores, then the full sums,
+    # log A and walk of those requests
+    t0 = time.time()
+    lp0, lq = oracle_rows(w, threads=threads)
+    sums = oracle.suffix_sums(lay, lp0, lq)
+    _, la = oracle.log_accept(sums, w.alpha)
+    oracle.walk(lay, la, w.u, w.max_steps)
+    dt = time.time() - t0
+    units = lay.suffix_tokens()
+    return {"value": units / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the whole batch ({w.n_rows} rows, {units} suffix tokens), "
+                      f"{dt:.1f} s wall on {threads} threads"}
+
+
+def reference_arm(args, ws, rank):
+    """--impl reference: the CPU oracle timed as the step, on bounded samples."""
+    if rank != 0:
+        return 0
+    import oracle
+    from synth import make_workload
+    from synth.trees import assemble_layout
+    w = make_workload(args.config, device="cpu") if args.config == 1 else None
+    if w is None:
+        # a bounded sample of the same batch: the same trees, with the rows of
+        # the first requests only (root rows + enough requests for ~1 s of work)
+        from synth.workload import CONFIGS, _trees_for, draw_tokens, gen_logits, Workload
+        cfg = dict(CONFIGS[args.config])
+        rng = np.random.default_rng(10086 + args.config)
+        tree = _trees_for(cfg, rng)[0]
+        keep = 1
+        rows = tree.T - tree.seg_cut[0]
+        while keep < len(tree.seg_cut) and rows + tree.T - tree.seg_cut[keep] <= 2500:
+            rows += tree.T - tree.seg_cut[keep]
+            keep += 1
+        tree.seg_cut = tree.seg_cut[:keep]
+        tree.seg_src = tree.seg_src[:keep]
+        tree.req = [r if r < keep else -1 for r in tree.req]
+        lay = assemble_layout([tree])
+        x = gen_logits(cfg["logits"][0], cfg["logits"][1], lay.n_rows, cfg["V"], cfg["dtype"],
+                       seed=1, device="cpu")
+        tok = draw_tokens(x, cfg["tau"], seed=2)
+        w = Workload(name=cfg["name"], layout=lay, V=cfg["V"], dtype=cfg["dtype"],
+                     alpha=cfg["alpha"], tau=cfg["tau"], logits=x, tokens=tok,
+                     u=1.0 - rng.random(lay.n_seg), max_steps=cfg["max_steps"])
+    from tests.helpers import logits_np
+    lg, dt = logits_np(w.logits)
+    toks = w.tokens.numpy()
+    threads = oracle.default_threads()
+
+    def step():
+        res = oracle.score_subtree(lg, dt, w.V, toks, w.layout, w.alpha, w.tau, threads=threads)
+        oracle.walk(w.layout, res["log_accept"], w.u, w.max_steps)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    el = time.time() - t0
+    units = w.layout.suffix_tokens() * args.steps
+    v = units / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_rows": w.n_rows,
+                       "sample_suffix_tokens": w.layout.suffix_tokens()},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{w.n_rows} rows of the batch per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="libps", choices=["libps", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, ws, rank)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import mh_prefetch_subtree_gb300 as ps
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = build_workload(args.config, dev, rank)
+    lay = w.layout
+    d = ps.DeviceSubtree.create(layout=lay, u=w.u, logits=w.logits, tokens=w.tokens, V=w.V,
+                                alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
+                                row_index=w.row_index, per_row=True, sums=True)
+    stream = torch.cuda.Stream(device=dev)
+    units_per_step = lay.suffix_tokens()
+    rows = w.n_rows
+    logits_bytes = w.logits_bytes()
+    alg_bytes_k1 = rows * (w.V * w.elem_bytes + 4 + 16)   # logits + token in, lp0/lq out
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            d.score_rows(stream)
+            d.assemble(stream)
+            d.walk(stream)
+    torch.cuda.synchronize()
+    st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
+    assert st == 0, ps.dev_status_names(st)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            d.score_rows(stream)
+            ev[i][1].record(stream)
+            d.assemble(stream)
+            d.walk(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks.stop()
+    total_ms = start.elapsed_time(end)
+    k1_ms = [a.elapsed_time(b) for a, b in ev]
+    k1_avg = sum(k1_ms) / len(k1_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = units_per_step * ws / (total_ms / 1e3 / args.steps)
+
+    # ---- end to end through the public API, host buffers ------------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_leg(ps, w, d, dev, stream, args, ws)
+
+    peak, peak_src = peaks()
+    achieved = alg_bytes_k1 / (k1_avg / 1e3) / 1e9
+    traffic = None
+    if NCU_TRAFFIC["source_sha1"] == kernel_source_sha1():
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded logits, BFS trees, proposal tokens drawn from q_tau)",
+        "config": {"workload": w.name, "V": w.V, "T": lay.T, "n_requests": lay.n_seg - lay.n_chains,
+                   "rows": rows, "suffix_tokens": units_per_step, "logits_bytes": logits_bytes,
+                   "alpha": w.alpha, "tau": w.tau,
+                   "l2": f"inputs {logits_bytes / 1e9:.1f} GB > 129 MB L2; no flush",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "kernel": "score_rows_kernel", "kernel_ms": k1_avg,
+                     "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
+        "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
+        "rows_per_s": rows * ws / (total_ms / 1e3 / args.steps),
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_leg(ps, w, d, dev, stream, args, ws):
+    """Same metric through ps_score_subtree + ps_walk_subtree, with the batch's
+    inputs copied from pinned host memory and the results read back, every step."""
+    lay = w.layout
+    h = {}
+    h["logits"] = torch.empty(w.logits.shape, dtype=w.logits.dtype, pin_memory=True)
+    h["logits"].copy_(w.logits)
+    h["tokens"] = w.tokens.cpu().pin_memory()
+    meta = {k: d.t[k] for k in ("chain_seg0", "seg_row0", "seg_cut", "seg_src", "chain_node0",
+                                "acc", "rej", "req", "u")}
+    hmeta = {k: v.cpu().pin_memory() for k, v in meta.items()}
+    outs = {k: d.t[k] for k in ("log_accept", "state_seg", "end_node", "k_delta", "path")}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = (h["logits"].numel() * h["logits"].element_size() + h["tokens"].numel() * 4
+           + sum(v.numel() * v.element_size() for v in hmeta.values()))
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def step():
+        w.logits.copy_(h["logits"], non_blocking=True)
+        w.tokens.copy_(h["tokens"], non_blocking=True)
+        for k, v in meta.items():
+            v.copy_(hmeta[k], non_blocking=True)
+        d.t["status"].zero_()
+        d.t["wstatus"].zero_()
+        d.score(stream)
+        d.walk(stream)
+        for k, v in outs.items():
+            hout[k].copy_(v, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = args.e2e_steps
+    if ws > 1:
+        torch.distributed.barrier()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(n):
+            step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    v = lay.suffix_tokens() * ws / (ms / 1e3 / n)
+    return {"value": v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": ms / n}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,269 @@
+/*
+ * ps.h -- C ABI of libps: scoring one prefetched subtree batch of PreSTO-style
+ * Metropolis-Hastings power sampling, and walking it, on one NVIDIA GB300 GPU.
+ *
+ * Method: "PreSTO: Predictive Subtree Prefetching for Fast LLM Power Sampling"
+ * (arXiv 2610.13171).  One prefetch round issues the feasible suffix-resampling
+ * requests of a subtree in a single batched call, scores them, and follows the
+ * realised accept/reject path (section 3.2, steps (2) and (3); Algorithm 2,
+ * PrefetchAndScore and MHTransition).
+ *
+ * Vocabulary of this header
+ *   position t      1..T; x_{0:c} is the prompt plus tokens 1..c, and a suffix
+ *                   resampled at cut c covers positions c+1..T (eq. (5)).
+ *   row             one scored position of one sequence: a row of V logits
+ *                   (the next-token distribution given tokens < t) and the
+ *                   token at t.
+ *   segment         the rows of one sequence's scored suffix.  Segment s covers
+ *                   positions seg_cut[s]+1..T in order, rows seg_row0[s] ..
+ *                   seg_row0[s+1]-1.  The first segment of every chain is the
+ *                   chain's current state x (its "root"); every other segment
+ *                   is one feasible request (v_i, c_i) with cut c_i = seg_cut[i].
+ *   src             for a request i, the segment whose proposal the state at the
+ *                   decision node came from: the nearest accepted request above
+ *                   the node, or the chain root.  Under Condition 1 that state
+ *                   is x_{0:c_src} followed by src's rows, so the x suffix of
+ *                   request i reads root rows for positions c_i+1..c_src and
+ *                   then all of src's rows (c_src = T for the root).
+ *   chain           one independent subtree.  Chains share nothing.
+ *
+ * Ownership: every pointer passed to the GPU calls is device memory owned by
+ * the caller, including the workspace.  The library allocates no device
+ * memory, keeps no per-call state and is safe to call from several host
+ * threads on different streams.  Calls are asynchronous on the given stream
+ * (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *
+ * Errors: the returned ps_status reports what the host can check without
+ * reading device memory (sizes, null pointers, alignment, launch failures).
+ * What only the device can see is reported as bits OR-ed into the caller's
+ * device int32 status word (PS_DEV_*); read it after synchronising.  The
+ * kernels never trap: a row or request that fails a device check gets NaN
+ * outputs and the walk treats a NaN log A as a rejection.
+ */
+#ifndef PS_H
+#define PS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PS_OK = 0,
+    PS_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, bad parameter */
+    PS_ERR_INFEASIBLE = 2,    /* a request violates Condition 1 (c_i > c_src) */
+    PS_ERR_BAD_TREE = 3,      /* tree arrays inconsistent (child/segment ids, cycles) */
+    PS_ERR_UNSUPPORTED = 4,   /* dtype or device not supported */
+    PS_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    PS_ERR_TIMEOUT = 6,       /* reserved: device waits report PS_DEV_TIMEOUT */
+    PS_ERR_WORKSPACE = 7      /* workspace null, misaligned or too small */
+} ps_status;
+
+typedef enum { PS_BF16 = 0, PS_F32 = 1 } ps_dtype;
+
+/* Device status bits (OR-ed into the caller's int32 status word). */
+#define PS_DEV_BAD_TOKEN     0x01  /* a token id outside [0, V) */
+#define PS_DEV_NONFINITE     0x02  /* a NaN or +inf logit (row result is NaN) */
+#define PS_DEV_INFEASIBLE    0x04  /* c_i > c_src, or c_i below the root's first row */
+#define PS_DEV_BAD_TREE      0x08  /* walk: bad child/segment id, or a path longer than the tree */
+#define PS_DEV_BAD_LAYOUT    0x10  /* segment sizes, row ranges or src ids inconsistent */
+#define PS_DEV_TIMEOUT       0x20  /* a bounded wait on a bulk copy gave up */
+#define PS_DEV_BAD_ROW_INDEX 0x40  /* row_index outside [0, n_logit_rows) */
+#define PS_DEV_BAD_UNIFORM   0x80  /* walk: an acceptance uniform outside (0, 1] */
+
+/* Request codes of a tree node's `req` entry. */
+#define PS_NODE_LEAF     (-1)     /* not expanded: the walk stops here */
+#define PS_NODE_DEFERRED (-2)     /* its request was deferred: the walk stops here */
+
+/*
+ * One subtree batch to score (section 3.2 step (2); eq. (6)).
+ *
+ * logits       [n_logit_rows][ld] row-major, dtype; base 16-byte aligned and
+ *              ld * element size a multiple of 16 bytes with
+ *              ld * element size >= V * element size rounded up to 16.
+ *              Elements V..ld-1 of a row are ignored.  -inf is a valid logit
+ *              (a masked token); NaN and +inf are reported as PS_DEV_NONFINITE.
+ * row_index    [n_rows] int64 or NULL: scored row r reads logits row
+ *              row_index[r]; NULL means row r reads logits row r (then
+ *              n_logit_rows >= n_rows).
+ * tokens       [n_rows] int32: the token at the row's position.
+ * chain_seg0   [n_chains+1] CSR offsets into segments; chain c owns segments
+ *              chain_seg0[c] .. chain_seg0[c+1]-1 and the first is its root.
+ * seg_row0     [n_seg+1] int64 CSR offsets into rows, seg_row0[n_seg] == n_rows,
+ *              seg_row0[s+1] - seg_row0[s] == T - seg_cut[s].
+ * seg_cut      [n_seg]: requests 0 <= c_i <= T-1 and c_i >= the chain root's
+ *              cut; a root's cut is the position before its first row (0..T).
+ * seg_src      [n_seg]: -1 for a chain root; for request i a segment of the
+ *              same chain other than i (the chain root's id when the decision
+ *              node holds the current state); c_i <= c_src (Condition 1).
+ * alpha, tau   power exponent (finite) and proposal temperature (> 0).
+ */
+typedef struct {
+    int32_t V;
+    int32_t T;
+    int32_t dtype;          /* ps_dtype */
+    int32_t n_chains;
+    int32_t n_seg;
+    int32_t reserved0;      /* must be 0 */
+    int64_t n_rows;
+    int64_t ld;
+    int64_t n_logit_rows;
+    double alpha;
+    double tau;
+    const int32_t *chain_seg0;
+    const int64_t *seg_row0;
+    const int32_t *seg_cut;
+    const int32_t *seg_src;
+    const void *logits;
+    const int64_t *row_index;
+    const int32_t *tokens;
+} ps_subtree_batch;
+
+/*
+ * Outputs of ps_score_subtree (all device memory, float64).  Entries of chain
+ * roots are set to NaN.
+ * lp0, lq      [n_rows] optional (NULL = not returned): log p0(token) and
+ *              log q_tau(token) of every row (Appendix B.1; Appendix D.3).
+ * lp_y, lq_y   [n_seg] optional: log p0 / log q_tau of the proposal suffix
+ *              y_{c_i+1:T} given x_{0:c_i}.
+ * lp_x, lq_x   [n_seg] optional: the same for the current suffix x_{c_i+1:T}.
+ * log_ratio    [n_seg] optional: r_i = (lq_x - lq_y) + alpha (lp_y - lp_x).
+ * log_accept   [n_seg] required: log A_i = min{0, r_i} (eq. (6)).
+ * status       device int32 word, required; the caller zeroes it.
+ */
+typedef struct {
+    double *lp0;
+    double *lq;
+    double *lp_y;
+    double *lq_y;
+    double *lp_x;
+    double *lq_x;
+    double *log_ratio;
+    double *log_accept;
+    int32_t *status;
+} ps_score_out;
+
+/*
+ * Bytes of device workspace ps_score_subtree needs for this batch (depends
+ * only on n_rows).  The workspace is scratch: per-row results when lp0/lq are
+ * not requested, partial sums of rows that are split across warps, and their
+ * arrival counters.  Returns 0 if batch is NULL.
+ */
+size_t ps_score_workspace_bytes(const ps_subtree_batch *batch);
+
+/*
+ * Score one subtree batch (section 3.2 step (2); eq. (6); Appendix B.1).
+ *
+ * For every row: log p0 and log q_tau of its token from the same logits, at
+ * temperature 1 and tau, in one pass over the row.  For every request i:
+ * suffix sums over its own rows (y) and over the rows of its from-state
+ * x_{0:c_src} + src (x), then r_i and log A_i = min{0, r_i}.
+ *
+ * workspace    device memory, 256-byte aligned, >= ps_score_workspace_bytes().
+ * cuda_stream  cudaStream_t or NULL.
+ * Returns PS_OK once the work is enqueued; see the header comment for errors.
+ */
+ps_status ps_score_subtree(const ps_subtree_batch *batch, const ps_score_out *out,
+                           void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * The two halves of ps_score_subtree, for callers that want per-token scores
+ * only or time the halves separately.
+ *
+ * ps_score_rows: log p0 and log q_tau of every row's token (Appendix B.1;
+ * Appendix D.3).  Reads only V, dtype, tau, n_rows, ld, n_logit_rows, logits,
+ * row_index and tokens of the batch.  lp0, lq: [n_rows] device float64,
+ * required.  status: device int32 word, required.  workspace as for
+ * ps_score_subtree (its per-row area is unused here).
+ *
+ * ps_assemble_subtree: suffix sums and log A of every request from per-row
+ * values lp0 / lq already computed for the batch's rows (eq. (6)).  Reads the
+ * segment arrays, T, alpha and n_rows of the batch; out->lp0 and out->lq are
+ * ignored.
+ */
+ps_status ps_score_rows(const ps_subtree_batch *batch, double *lp0, double *lq, int32_t *status,
+                        void *workspace, size_t workspace_bytes, void *cuda_stream);
+ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
+                              const double *lq, const ps_score_out *out, void *cuda_stream);
+
+/*
+ * The prefetched subtree of every chain, for the walk (section 3.2 step (3)).
+ * Node ids and segment ids are global (the same numbering as the batch).
+ * chain_node0  [n_chains+1] CSR offsets into nodes; the first node of a chain
+ *              is its root v0.
+ * chain_seg0   [n_chains+1] as in ps_subtree_batch (the root segment of chain c
+ *              is chain_seg0[c]).
+ * acc, rej     [n_nodes] acceptance / rejection child node id, or -1.
+ * req          [n_nodes] the request whose proposal the decision at the node
+ *              uses (a segment id of the chain), PS_NODE_LEAF or
+ *              PS_NODE_DEFERRED.
+ * u            [n_seg] acceptance uniform of each request, in (0, 1]; deferred
+ *              requests keep theirs for a later round, so none is consumed.
+ * max_steps    K - k: at most this many transitions (>= 0).
+ */
+typedef struct {
+    int32_t n_chains;
+    int32_t n_nodes;
+    int32_t n_seg;
+    int32_t max_steps;
+    const int32_t *chain_node0;
+    const int32_t *chain_seg0;
+    const int32_t *acc;
+    const int32_t *rej;
+    const int32_t *req;
+    const double *u;
+} ps_tree;
+
+/*
+ * Outputs of ps_walk_subtree (device int32 arrays, [n_chains] each).
+ * state_seg    segment of the reached state: the last accepted request, or
+ *              the chain root when nothing was accepted (x_Delta).
+ * end_node     node where the walk stopped.
+ * k_delta      transitions completed (every visited scored decision counts,
+ *              accepted or rejected; Definition 1).
+ * path         optional [n_chains][max_steps+1]: node ids visited, root first,
+ *              then -1 padding.
+ * status       device int32 word, required; the caller zeroes it.
+ */
+typedef struct {
+    int32_t *state_seg;
+    int32_t *end_node;
+    int32_t *k_delta;
+    int32_t *path;
+    int32_t *status;
+} ps_walk_out;
+
+/*
+ * Walk every chain's subtree from its root (section 3.2 step (3); Example 5;
+ * Algorithm 2 MHTransition).  At a node whose request was scored, one
+ * transition: move to the acceptance child if log u <= log A (u <= A,
+ * Algorithm 1 line 7), else to the rejection child.  Stop at a leaf, at a node
+ * whose request was deferred, or after max_steps transitions.
+ * log_accept   [n_seg] device float64, as written by ps_score_subtree.
+ */
+ps_status ps_walk_subtree(const ps_tree *tree, const double *log_accept,
+                          const ps_walk_out *out, void *cuda_stream);
+
+/*
+ * Full structural check of a batch and its tree in HOST memory (synchronous;
+ * reads no logits).  Either argument may be NULL to skip it.  When both are
+ * given, also checks that each request's src is the state of its decision
+ * node.  Writes a one-line reason into msg (if msg_len > 0) on failure.
+ * Returns PS_OK, PS_ERR_INVALID_ARG, PS_ERR_INFEASIBLE or PS_ERR_BAD_TREE.
+ */
+ps_status ps_validate_subtree(const ps_subtree_batch *batch, const ps_tree *tree,
+                              char *msg, size_t msg_len);
+
+/* Static text for a status code. */
+const char *ps_status_string(ps_status status);
+
+/* Library version string. */
+const char *ps_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PS_H */

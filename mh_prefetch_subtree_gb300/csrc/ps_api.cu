@@ -1,0 +1,381 @@
+// Host side of libps: argument checks, workspace layout, launches, and the
+// synchronous structural validator.  See include/ps.h for the contract.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "ps_internal.cuh"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t rows_off, rows_bytes;
+    size_t parts_off, parts_bytes;
+    size_t cnt_off, cnt_bytes;
+    size_t total;
+};
+
+WsLayout ws_layout(int64_t n_rows) {
+    WsLayout w;
+    w.rows_off = 0;
+    w.rows_bytes = align_up((size_t)(n_rows > 0 ? n_rows : 0) * 2 * sizeof(double), kAlign);
+    w.parts_off = w.rows_off + w.rows_bytes;
+    w.parts_bytes = align_up((size_t)2 * ps::kMaxWarps * sizeof(ps::RowPart), kAlign);
+    w.cnt_off = w.parts_off + w.parts_bytes;
+    w.cnt_bytes = align_up((size_t)ps::kMaxWarps * sizeof(int32_t), kAlign);
+    w.total = w.cnt_off + w.cnt_bytes;
+    return w;
+}
+
+int elem_size(int32_t dtype) { return dtype == PS_BF16 ? 2 : (dtype == PS_F32 ? 4 : 0); }
+
+// Device that owns `ptr`, made current for this thread; SM count cached.
+ps_status device_of(const void *ptr, int *sms) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return PS_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return PS_ERR_INVALID_ARG;
+    const int dev = attr.device;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return PS_ERR_CUDA;
+    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return PS_ERR_CUDA;
+    static std::mutex mu;
+    static std::vector<int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PS_ERR_CUDA;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major * 10 + minor != 103) return PS_ERR_UNSUPPORTED;   // built for sm_103a only
+        cache[dev] = n;
+    }
+    *sms = cache[dev];
+    return PS_OK;
+}
+
+ps_status map_cuda(cudaError_t e) { return e == cudaSuccess ? PS_OK : PS_ERR_CUDA; }
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// 1/tau when it is exactly 1, 2, 4 or 8 (then the tau exponential is a power).
+int32_t integer_power(double tau) {
+    const double g = 1.0 / tau;
+    for (int n : {1, 2, 4, 8})
+        if (g == (double)n) return n;
+    return 0;
+}
+
+ps_status check_batch_host(const ps_subtree_batch *b, bool need_data = true) {
+    if (!b) return PS_ERR_INVALID_ARG;
+    if (b->V < 1 || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)
+        return PS_ERR_INVALID_ARG;
+    if (b->reserved0 != 0) return PS_ERR_INVALID_ARG;
+    const int esz = elem_size(b->dtype);
+    if (esz == 0) return PS_ERR_UNSUPPORTED;
+    if (!(b->tau > 0.0) || !isfinite(b->tau) || !isfinite(b->alpha)) return PS_ERR_INVALID_ARG;
+    const int64_t row_bytes = ((int64_t)b->V * esz + 15) / 16 * 16;
+    if (b->ld < b->V || (b->ld * esz) % 16 != 0 || b->ld * esz < row_bytes)
+        return PS_ERR_INVALID_ARG;
+    if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
+    if (b->n_rows > 0 && need_data) {
+        if (!b->logits || !b->tokens || !aligned(b->logits, 16)) return PS_ERR_INVALID_ARG;
+        if (b->row_index) {
+            if (b->n_logit_rows < 1) return PS_ERR_INVALID_ARG;
+        } else if (b->n_logit_rows < b->n_rows) {
+            return PS_ERR_INVALID_ARG;
+        }
+    }
+    return PS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ps_version(void) { return "libps 0.1.0 (sm_103a)"; }
+
+const char *ps_status_string(ps_status s) {
+    switch (s) {
+        case PS_OK: return "ok";
+        case PS_ERR_INVALID_ARG: return "invalid argument";
+        case PS_ERR_INFEASIBLE: return "request violates Condition 1 (c_i > c_src)";
+        case PS_ERR_BAD_TREE: return "inconsistent tree";
+        case PS_ERR_UNSUPPORTED: return "unsupported dtype or device";
+        case PS_ERR_CUDA: return "CUDA runtime error";
+        case PS_ERR_TIMEOUT: return "device wait timed out";
+        case PS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
+    if (!batch) return 0;
+    return ws_layout(batch->n_rows).total;
+}
+
+ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, int32_t *status,
+                        void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(b->n_rows);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
+        return PS_ERR_WORKSPACE;
+    if (b->n_rows == 0) return PS_OK;
+    int sms = 0;
+    st = device_of(b->logits, &sms);
+    if (st != PS_OK) return st;
+    cudaStream_t stream = (cudaStream_t)cuda_stream;
+    uint8_t *ws = (uint8_t *)workspace;
+    const int esz = elem_size(b->dtype);
+    ps::RowsParams p;
+    p.logits = (const uint8_t *)b->logits;
+    p.ld_bytes = b->ld * esz;
+    p.n_logit_rows = b->row_index ? b->n_logit_rows : b->n_rows;
+    p.row_index = b->row_index;
+    p.tokens = b->tokens;
+    p.n_rows = b->n_rows;
+    p.V = b->V;
+    p.dtype = b->dtype;
+    p.row_bytes = (int32_t)(((int64_t)b->V * esz + 15) / 16 * 16);
+    p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
+    p.n_chunks = b->n_rows * p.cpr;
+    int64_t warps = (int64_t)sms * ps::kWarpsPerCta;
+    if (warps > ps::kMaxWarps) warps = ps::kMaxWarps;
+    if (warps > p.n_chunks) warps = p.n_chunks;
+    p.n_vwarps = (int32_t)warps;
+    p.npow = integer_power(b->tau);
+    p.g = (float)(1.0 / b->tau);
+    p.lp0 = lp0;
+    p.lq = lq;
+    p.parts = (ps::RowPart *)(ws + wl.parts_off);
+    p.counters = (int32_t *)(ws + wl.cnt_off);
+    p.status = status;
+    const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
+    st = map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
+    if (st != PS_OK) return st;
+    return map_cuda(ps::launch_score_rows(p, n_ctas, stream));
+}
+
+ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, const double *lq,
+                              const ps_score_out *out, void *cuda_stream) {
+    if (!b || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0 ||
+        !isfinite(b->alpha))
+        return PS_ERR_INVALID_ARG;
+    if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
+    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    if (b->n_rows > 0 && (!lp0 || !lq)) return PS_ERR_INVALID_ARG;
+    int sms = 0;
+    ps_status st = device_of(out->log_accept, &sms);
+    if (st != PS_OK) return st;
+    ps::AssembleParams a;
+    a.T = b->T;
+    a.n_chains = b->n_chains;
+    a.n_seg = b->n_seg;
+    a.n_rows = b->n_rows;
+    a.alpha = b->alpha;
+    a.chain_seg0 = b->chain_seg0;
+    a.seg_row0 = b->seg_row0;
+    a.seg_cut = b->seg_cut;
+    a.seg_src = b->seg_src;
+    a.lp0 = lp0;
+    a.lq = lq;
+    a.lp_y = out->lp_y;
+    a.lq_y = out->lq_y;
+    a.lp_x = out->lp_x;
+    a.lq_x = out->lq_x;
+    a.log_ratio = out->log_ratio;
+    a.log_accept = out->log_accept;
+    a.status = out->status;
+    return map_cuda(ps::launch_assemble(a, (cudaStream_t)cuda_stream));
+}
+
+ps_status ps_score_subtree(const ps_subtree_batch *b, const ps_score_out *out, void *workspace,
+                           size_t workspace_bytes, void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(b->n_rows);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
+        return PS_ERR_WORKSPACE;
+    uint8_t *ws = (uint8_t *)workspace;
+    double *lp0 = out->lp0 ? out->lp0 : (double *)(ws + wl.rows_off);
+    double *lq = out->lq ? out->lq : (double *)(ws + wl.rows_off) + b->n_rows;
+    st = ps_score_rows(b, lp0, lq, out->status, workspace, workspace_bytes, cuda_stream);
+    if (st != PS_OK) return st;
+    return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
+}
+
+ps_status ps_walk_subtree(const ps_tree *t, const double *log_accept, const ps_walk_out *out,
+                          void *cuda_stream) {
+    if (!t || !log_accept || !out) return PS_ERR_INVALID_ARG;
+    if (t->n_chains < 1 || t->n_nodes < t->n_chains || t->n_seg < t->n_chains ||
+        t->max_steps < 0)
+        return PS_ERR_INVALID_ARG;
+    if (!t->chain_node0 || !t->chain_seg0 || !t->acc || !t->rej || !t->req || !t->u)
+        return PS_ERR_INVALID_ARG;
+    if (!out->state_seg || !out->end_node || !out->k_delta || !out->status)
+        return PS_ERR_INVALID_ARG;
+    int sms = 0;
+    ps_status st = device_of(log_accept, &sms);
+    if (st != PS_OK) return st;
+    ps::WalkParams p;
+    p.n_chains = t->n_chains;
+    p.n_nodes = t->n_nodes;
+    p.n_seg = t->n_seg;
+    p.max_steps = t->max_steps;
+    p.chain_node0 = t->chain_node0;
+    p.chain_seg0 = t->chain_seg0;
+    p.acc = t->acc;
+    p.rej = t->rej;
+    p.req = t->req;
+    p.u = t->u;
+    p.log_accept = log_accept;
+    p.state_seg = out->state_seg;
+    p.end_node = out->end_node;
+    p.k_delta = out->k_delta;
+    p.path = out->path;
+    p.status = out->status;
+    return map_cuda(ps::launch_walk(p, (cudaStream_t)cuda_stream));
+}
+
+ps_status ps_validate_subtree(const ps_subtree_batch *b, const ps_tree *t, char *msg,
+                              size_t msg_len) {
+    auto fail = [&](ps_status s, const char *fmt, long long a, long long c) {
+        if (msg && msg_len) snprintf(msg, msg_len, fmt, a, c);
+        return s;
+    };
+    if (msg && msg_len) msg[0] = 0;
+    if (b) {
+        ps_status s = check_batch_host(b, false);
+        if (s != PS_OK) return fail(s, "batch header invalid (%lld %lld)", s, 0);
+        const int32_t T = b->T;
+        if (b->chain_seg0[0] != 0 || b->chain_seg0[b->n_chains] != b->n_seg)
+            return fail(PS_ERR_INVALID_ARG, "chain_seg0 must run 0..n_seg (%lld, %lld)",
+                        b->chain_seg0[0], b->chain_seg0[b->n_chains]);
+        if (b->seg_row0[0] != 0 || b->seg_row0[b->n_seg] != b->n_rows)
+            return fail(PS_ERR_INVALID_ARG, "seg_row0 must run 0..n_rows (%lld, %lld)",
+                        (long long)b->seg_row0[0], (long long)b->seg_row0[b->n_seg]);
+        for (int32_t c = 0; c < b->n_chains; ++c) {
+            const int32_t s0 = b->chain_seg0[c], s1 = b->chain_seg0[c + 1];
+            if (s1 <= s0) return fail(PS_ERR_INVALID_ARG, "chain %lld has no root (%lld)", c, s1);
+            const int32_t rc = b->seg_cut[s0];
+            if (b->seg_src[s0] != -1 || rc < 0 || rc > T)
+                return fail(PS_ERR_INVALID_ARG, "chain %lld root segment %lld invalid", c, s0);
+            for (int32_t s = s0; s < s1; ++s) {
+                const int64_t n = b->seg_row0[s + 1] - b->seg_row0[s];
+                if (n != (int64_t)(T - b->seg_cut[s]))
+                    return fail(PS_ERR_INVALID_ARG, "segment %lld has %lld rows, not T - cut", s, n);
+                if (s == s0) continue;
+                const int32_t cs = b->seg_cut[s], src = b->seg_src[s];
+                if (cs < 0 || cs > T - 1)
+                    return fail(PS_ERR_INVALID_ARG, "request %lld cut %lld outside 0..T-1", s, cs);
+                if (src < s0 || src >= s1 || src == s)
+                    return fail(PS_ERR_INVALID_ARG, "request %lld src %lld not in its chain", s,
+                                src);
+                const int32_t csrc = src == s0 ? T : b->seg_cut[src];
+                if (cs > csrc)
+                    return fail(PS_ERR_INFEASIBLE, "request %lld: c_i > c_src (%lld)", s, csrc);
+                if (cs < rc)
+                    return fail(PS_ERR_INFEASIBLE, "request %lld cut below root rows (%lld)", s,
+                                rc);
+            }
+        }
+        if (b->tokens && b->n_rows > 0) {
+            for (int64_t r = 0; r < b->n_rows; ++r)
+                if (b->tokens[r] < 0 || b->tokens[r] >= b->V)
+                    return fail(PS_ERR_INVALID_ARG, "row %lld token %lld outside [0, V)", r,
+                                b->tokens[r]);
+        }
+        if (b->row_index && b->n_rows > 0) {
+            for (int64_t r = 0; r < b->n_rows; ++r)
+                if (b->row_index[r] < 0 || b->row_index[r] >= b->n_logit_rows)
+                    return fail(PS_ERR_INVALID_ARG, "row %lld row_index %lld out of range", r,
+                                (long long)b->row_index[r]);
+        }
+    }
+    if (t) {
+        if (t->n_chains < 1 || t->max_steps < 0 || !t->chain_node0 || !t->chain_seg0 ||
+            !t->acc || !t->rej || !t->req)
+            return fail(PS_ERR_INVALID_ARG, "tree header invalid (%lld %lld)", t->n_chains,
+                        t->max_steps);
+        if (b && (t->n_chains != b->n_chains || t->n_seg != b->n_seg))
+            return fail(PS_ERR_INVALID_ARG, "tree and batch disagree (%lld chains, %lld segs)",
+                        t->n_chains, t->n_seg);
+        if (t->chain_node0[0] != 0 || t->chain_node0[t->n_chains] != t->n_nodes)
+            return fail(PS_ERR_BAD_TREE, "chain_node0 must run 0..n_nodes (%lld %lld)",
+                        t->chain_node0[0], t->chain_node0[t->n_chains]);
+        for (int32_t c = 0; c < t->n_chains; ++c) {
+            const int32_t n0 = t->chain_node0[c], n1 = t->chain_node0[c + 1];
+            const int32_t s0 = t->chain_seg0[c], s1 = t->chain_seg0[c + 1];
+            if (n1 <= n0 || s1 <= s0)
+                return fail(PS_ERR_BAD_TREE, "chain %lld empty (%lld)", c, n1 - n0);
+            // parent count, reachability and state of every node, from the root
+            std::vector<int32_t> parents(n1 - n0, 0), state(n1 - n0, -3);
+            std::vector<int32_t> used_req(s1 - s0, 0);
+            for (int32_t v = n0; v < n1; ++v) {
+                const int32_t kids[2] = {t->acc[v], t->rej[v]};
+                for (int32_t ch : kids) {
+                    if (ch == -1) continue;
+                    if (ch <= n0 || ch >= n1)
+                        return fail(PS_ERR_BAD_TREE, "node %lld child %lld out of chain", v, ch);
+                    if (++parents[ch - n0] > 1)
+                        return fail(PS_ERR_BAD_TREE, "node %lld has two parents (%lld)", ch, v);
+                }
+                const int32_t q = t->req[v];
+                if (q >= 0) {
+                    if (q <= s0 || q >= s1)
+                        return fail(PS_ERR_BAD_TREE, "node %lld request %lld not in chain", v, q);
+                    if (used_req[q - s0]++)
+                        return fail(PS_ERR_BAD_TREE, "request %lld used twice (node %lld)", q, v);
+                    if (t->acc[v] < 0 || t->rej[v] < 0)
+                        return fail(PS_ERR_BAD_TREE, "node %lld has a request but no children %lld",
+                                    v, q);
+                } else if (q != PS_NODE_LEAF && q != PS_NODE_DEFERRED) {
+                    return fail(PS_ERR_BAD_TREE, "node %lld request code %lld invalid", v, q);
+                }
+            }
+            if (parents[0] != 0) return fail(PS_ERR_BAD_TREE, "root of chain %lld has a parent %lld", c, 0);
+            // forward pass in an order where parents come first
+            std::vector<int32_t> order;
+            order.push_back(n0);
+            state[0] = s0;
+            for (size_t i = 0; i < order.size(); ++i) {
+                const int32_t v = order[i];
+                const int32_t q = t->req[v];
+                if (t->rej[v] >= 0) {
+                    state[t->rej[v] - n0] = state[v - n0];
+                    order.push_back(t->rej[v]);
+                }
+                if (t->acc[v] >= 0) {
+                    state[t->acc[v] - n0] = q >= 0 ? q : -2;   // -2: no generated state
+                    if (q >= 0) order.push_back(t->acc[v]);
+                    if (b && q >= 0 && b->seg_src[q] != state[v - n0])
+                        return fail(PS_ERR_BAD_TREE,
+                                    "request %lld: seg_src is not its decision node's state %lld",
+                                    q, state[v - n0]);
+                }
+            }
+            for (int32_t v = n0; v < n1; ++v)
+                if (state[v - n0] == -3)
+                    return fail(PS_ERR_BAD_TREE, "node %lld unreachable from the root (%lld)", v, c);
+        }
+    }
+    return PS_OK;
+}
+
+}  // extern "C"

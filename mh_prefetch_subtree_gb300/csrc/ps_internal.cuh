@@ -1,0 +1,173 @@
+// Internal declarations shared by the libps translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ps.h"
+
+namespace ps {
+
+// ---------------------------------------------------------------------------
+// Scoring kernel geometry (K1).  Each warp streams its own contiguous range of
+// row chunks through a private ring of shared-memory stages filled by 1-D bulk
+// copies; see ps_score_rows.cu.
+// ---------------------------------------------------------------------------
+constexpr int kWarpsPerCta = 16;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 4096;
+constexpr int kMaxCtas = 2048;                        // workspace sizing bound
+constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
+
+// Partial log-sum-exp state of (part of) a row: sums of 2^(l*log2e - R) and
+// 2^(g*(l*log2e - R)) over the row's elements except the token, plus the
+// token's logit when this part held it (NaN otherwise).
+struct __align__(16) RowPart {
+    float R;
+    float s1;
+    float st;
+    float ltok;
+};
+
+struct RowsParams {
+    const uint8_t *logits;
+    int64_t ld_bytes;
+    int64_t n_logit_rows;
+    const int64_t *row_index;
+    const int32_t *tokens;
+    int64_t n_rows;
+    int32_t V;
+    int32_t dtype;              // PS_BF16 / PS_F32
+    int32_t row_bytes;          // V * elem rounded up to 16
+    int32_t cpr;                // chunks per row
+    int64_t n_chunks;           // n_rows * cpr
+    int32_t n_vwarps;           // warps that own a non-empty chunk range
+    int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; else 0
+    float g;                    // 1/tau in float
+    double *lp0;
+    double *lq;
+    RowPart *parts;             // [2 * kMaxWarps]
+    int32_t *counters;          // [kMaxWarps]
+    int32_t *status;
+};
+
+struct AssembleParams {
+    int32_t T;
+    int32_t n_chains;
+    int32_t n_seg;
+    int64_t n_rows;
+    double alpha;
+    const int32_t *chain_seg0;
+    const int64_t *seg_row0;
+    const int32_t *seg_cut;
+    const int32_t *seg_src;
+    const double *lp0;
+    const double *lq;
+    double *lp_y, *lq_y, *lp_x, *lq_x, *log_ratio, *log_accept;
+    int32_t *status;
+};
+
+struct WalkParams {
+    int32_t n_chains;
+    int32_t n_nodes;
+    int32_t n_seg;
+    int32_t max_steps;
+    const int32_t *chain_node0;
+    const int32_t *chain_seg0;
+    const int32_t *acc, *rej, *req;
+    const double *u;
+    const double *log_accept;
+    int32_t *state_seg, *end_node, *k_delta, *path;
+    int32_t *status;
+};
+
+// Launchers (host side, asynchronous on `stream`).
+cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream);
+cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
+cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);
+size_t score_rows_smem_bytes();
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: spins on try_wait (which itself suspends for a short,
+// hardware-chosen time) and gives up after `limit_ns` of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Hardware base-2 exponential (MUFU), flush-to-zero.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace ps

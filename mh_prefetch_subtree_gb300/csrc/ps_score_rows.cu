@@ -1,0 +1,526 @@
+// K1: per-token log p0 and log q_tau of every scored row, in one pass over
+// the row's logits (PreSTO, Appendix B.1 last paragraph and Appendix D.3:
+// both log-probabilities come from the same logits, without and with the
+// temperature).
+//
+// Formulation.  For a row l_0..l_{V-1} with token k, and any reference R
+// (log2 units), with L = log2(e) and g = 1/tau:
+//     S1 = sum_{j != k} 2^(l_j L - R),   St = sum_{j != k} 2^(g (l_j L - R)),
+//     t  = l_k L - R,
+//     log p0(k)    = -ln(1 + S1 2^-t),  log q_tau(k) = -ln(1 + St 2^(-g t)).
+// This is log softmax written relative to the token itself, so the token is
+// left out of both sums and the result keeps its relative accuracy when the
+// token holds nearly all the mass (the sums are then tiny, never 1 + tiny).
+// No maximum is needed: R only has to keep the exponentials in range.  Each
+// lane starts with R = -inf; a chunk whose sums overflow (or are NaN) takes a
+// slow path that raises R to the chunk's maximum and rescales.  When 1/tau is
+// 1, 2, 4 or 8 the tau exponential is the first one squared, so each logit
+// costs one MUFU ex2.
+//
+// Data movement.  The rows are cut into 4 KB chunks (the last chunk of a row
+// may be shorter).  The chunk sequence of all rows is split into contiguous
+// ranges, one per warp, so every warp streams about the same number of bytes
+// whatever the row count.  Each warp owns a ring of 3 shared-memory stages that
+// its lane 0 fills with 1-D bulk copies (cp.async.bulk, completion on an
+// mbarrier); the warp consumes a stage, refills it, and moves on.  There is no
+// block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
+// row's token logit (after saving it) and any padding beyond V with -inf.
+//
+// A row whose chunks all lie in one warp's range is finalised by that warp.
+// A row split across warps leaves one partial per warp in the workspace; the
+// last warp to arrive (atomic counter) merges them in warp order and
+// finalises.  Results are deterministic.
+#include <math.h>
+
+#include "ps_internal.cuh"
+
+namespace ps {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2f = 0.6931471805599453f;
+constexpr float kLimit = 1.8446744073709552e19f;   // 2^64: largest chunk sum kept as is
+constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s for one bulk copy
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kVecPerStage = kStageBytes / 16;     // 256 x 16 B
+constexpr int kVecPerLane = kVecPerStage / 32;     // 8
+constexpr uint32_t kAbsent = 0x7fc0deadu;           // "token not in this part" (a NaN payload
+                                                    // no bf16/f32 logit converts to)
+
+__device__ __forceinline__ int64_t range_begin(int64_t w, int64_t C, int64_t W) {
+    return (w * C) / W;
+}
+
+// The warp whose chunk range holds chunk c (all ranges are non-empty: W <= C).
+__device__ __forceinline__ int64_t warp_of_chunk(int64_t c, int64_t C, int64_t W) {
+    int64_t w = (c * W) / C;
+    if (w >= W) w = W - 1;
+    while (w + 1 < W && range_begin(w + 1, C, W) <= c) ++w;
+    while (w > 0 && range_begin(w, C, W) > c) --w;
+    return w;
+}
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<PS_BF16> {
+    static constexpr int kSize = 2;
+    static constexpr uint32_t kNegInfWord = 0xff80ff80u;
+};
+template <>
+struct Elem<PS_F32> {
+    static constexpr int kSize = 4;
+    static constexpr uint32_t kNegInfWord = 0xff800000u;
+};
+
+// One pair of logits: accumulate 2^(x) into a1 and 2^(g x) into at.
+template <int NP>
+__device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2, float2 &a1,
+                                      float2 &at) {
+    const float2 x = __ffma2_rn(v, L2, nR2);
+    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+    a1 = __fadd2_rn(a1, e);
+    if constexpr (NP == 2) {
+        at = __fadd2_rn(at, __fmul2_rn(e, e));
+    } else if constexpr (NP == 4) {
+        const float2 e2 = __fmul2_rn(e, e);
+        at = __fadd2_rn(at, __fmul2_rn(e2, e2));
+    } else if constexpr (NP == 8) {
+        const float2 e2 = __fmul2_rn(e, e);
+        const float2 e4 = __fmul2_rn(e2, e2);
+        at = __fadd2_rn(at, __fmul2_rn(e4, e4));
+    } else if constexpr (NP == 0) {
+        const float2 xt = __fmul2_rn(x, G2);
+        at = __fadd2_rn(at, make_float2(ex2(xt.x), ex2(xt.y)));
+    }
+}
+
+// Sums of one lane's 8 vectors relative to reference R.
+template <int DT, int NP>
+__device__ __forceinline__ void sum_vecs(const uint4 (&q)[kVecPerLane], float R, float g,
+                                         float &c1, float &ct) {
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    const float2 nR2 = make_float2(-R, -R);
+    const float2 G2 = make_float2(g, g);
+    float2 a1[4], at[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        a1[j] = make_float2(0.f, 0.f);
+        at[j] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+        if constexpr (DT == PS_BF16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 v = make_float2(__uint_as_float(w[j] << 16),
+                                             __uint_as_float(w[j] & 0xffff0000u));
+                step2<NP>(v, L2, nR2, G2, a1[j], at[j]);
+            }
+        } else {
+            step2<NP>(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])), L2, nR2, G2,
+                      a1[(i & 1) * 2], at[(i & 1) * 2]);
+            step2<NP>(make_float2(__uint_as_float(w[2]), __uint_as_float(w[3])), L2, nR2, G2,
+                      a1[(i & 1) * 2 + 1], at[(i & 1) * 2 + 1]);
+        }
+    }
+    const float2 s01 = __fadd2_rn(a1[0], a1[1]), s23 = __fadd2_rn(a1[2], a1[3]);
+    const float2 s = __fadd2_rn(s01, s23);
+    c1 = s.x + s.y;
+    if constexpr (NP == 1) {
+        ct = c1;
+    } else {
+        const float2 t01 = __fadd2_rn(at[0], at[1]), t23 = __fadd2_rn(at[2], at[3]);
+        const float2 t = __fadd2_rn(t01, t23);
+        ct = t.x + t.y;
+    }
+}
+
+// Rescale factor for the tau sums when the reference moves by d (log2 units).
+template <int NP>
+__device__ __forceinline__ float tau_scale(float d, float g) {
+    if constexpr (NP == 0) return ex2(d * g);
+    else return ex2(d * (float)NP);
+}
+
+// Load one lane's 8 vectors of a stage; vectors past the chunk read as -inf.
+template <int DT>
+__device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
+                                          uint4 (&q)[kVecPerLane]) {
+    const uint32_t ni = Elem<DT>::kNegInfWord;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const int idx = lane + 32 * i;
+        q[i] = idx < nvec ? v4[idx] : make_uint4(ni, ni, ni, ni);
+    }
+}
+
+// Rare path: the chunk's sums overflowed or were NaN (always the case for a
+// lane's first chunk of a row, whose reference is still -inf).  Re-reads the
+// lane's vectors from shared memory, raises R to their maximum, rescales the
+// running sums and adds the chunk.
+template <int DT, int NP>
+__device__ __noinline__ float3 slow_chunk(const uint4 *v4, int nvec, int lane, float g, float R,
+                                          float s1, float st) {
+    uint4 q[kVecPerLane];
+    load_vecs<DT>(v4, nvec, lane, q);
+    float m = -INFINITY;
+    bool nan_seen = false;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (DT == PS_BF16) {
+                const float lo = __uint_as_float(w[j] << 16);
+                const float hi = __uint_as_float(w[j] & 0xffff0000u);
+                nan_seen |= (lo != lo) | (hi != hi);
+                m = fmaxf(m, fmaxf(lo, hi));
+            } else {
+                const float v = __uint_as_float(w[j]);
+                nan_seen |= (v != v);
+                m = fmaxf(m, v);
+            }
+        }
+    }
+    if (nan_seen) {
+        const float qn = __int_as_float(0x7fc00000);
+        return make_float3(R, qn, qn);
+    }
+    const float Rm = m * kLog2e;
+    const float Rn = fmaxf(R, Rm);
+    if (Rn == -INFINITY) return make_float3(R, s1, st);   // only -inf so far: nothing to add
+    if (Rn > R) {
+        const float d = R - Rn;    // -inf when R was -inf: the old sums are 0 anyway
+        s1 *= ex2(d);
+        if constexpr (NP != 1) st *= tau_scale<NP>(d, g);
+        R = Rn;
+    }
+    float c1, ct;
+    sum_vecs<DT, NP>(q, R, g, c1, ct);
+    s1 += c1;
+    if constexpr (NP != 1) st += ct;
+    return make_float3(R, s1, st);
+}
+
+// Merge partial b into a (both relative to their own reference).
+template <int NP>
+__device__ __forceinline__ void merge_part(float &R, float &s1, float &st, float Rb, float s1b,
+                                           float stb, float g) {
+    const float M = fmaxf(R, Rb);
+    if (M == -INFINITY) {          // both parts saw only -inf logits
+        s1 += s1b;                 // keeps a NaN poison, else 0
+        st += stb;
+        return;
+    }
+    const float da = R - M, db = Rb - M;
+    s1 = s1 * ex2(da) + s1b * ex2(db);
+    if constexpr (NP != 1) st = st * tau_scale<NP>(da, g) + stb * tau_scale<NP>(db, g);
+    R = M;
+}
+
+template <int NP>
+__device__ __forceinline__ void warp_merge(float &R, float &s1, float &st, float g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float Rb = __shfl_xor_sync(0xffffffffu, R, off);
+        const float s1b = __shfl_xor_sync(0xffffffffu, s1, off);
+        const float stb = __shfl_xor_sync(0xffffffffu, st, off);
+        merge_part<NP>(R, s1, st, Rb, s1b, stb, g);
+    }
+}
+
+// -ln(1 + 2^a) in float64 (the value is computed in float, except for the tiny
+// tail, whose magnitude is below float's range).
+__device__ __forceinline__ double neg_log1p_exp2(float a) {
+    if (a > 24.f) return -(double)(a * kLn2f + log1pf(exp2f(-a)));
+    if (a > -120.f) return -(double)log1pf(exp2f(a));
+    return -exp2((double)a);
+}
+
+template <int NP>
+__device__ void finalize_row(const RowsParams &p, int64_t r, float R, float s1, float st,
+                             float lt, bool bad) {
+    double o0, oq;
+    const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+    if (bad || __float_as_uint(lt) == kAbsent) {
+        o0 = oq = qnan;
+    } else {
+        const float t = fmaf(lt, kLog2e, -R);
+        const bool nonfinite = (lt != lt) || (lt == INFINITY) || (R != R) || (s1 != s1) ||
+                               (st != st) || (R == INFINITY) || (t != t);
+        if (nonfinite) {
+            set_status(p.status, PS_DEV_NONFINITE);
+            o0 = oq = qnan;
+        } else {
+            o0 = neg_log1p_exp2(s1 > 0.f ? log2f(s1) - t : -INFINITY);
+            if constexpr (NP == 1) {
+                oq = o0;
+            } else {
+                const float gt = (NP == 0) ? t * p.g : t * (float)NP;
+                oq = neg_log1p_exp2(st > 0.f ? log2f(st) - gt : -INFINITY);
+            }
+        }
+    }
+    p.lp0[r] = o0;
+    p.lq[r] = oq;
+}
+
+template <int DT, int NP>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 1) score_rows_kernel(const RowsParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kEsz = Elem<DT>::kSize;
+    constexpr int kElemsPerStage = kStageBytes / kEsz;
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int64_t W = p.n_vwarps;
+    const int64_t vw = (int64_t)blockIdx.x * kWarpsPerCta + wid;
+    if (vw >= W) return;
+    const int64_t C = p.n_chunks;
+    const int64_t cb = range_begin(vw, C, W);
+    const int64_t ce = range_begin(vw + 1, C, W);
+    const int32_t cpr = p.cpr;
+    const float g = p.g;
+
+    uint8_t *stage = smem + (size_t)wid * kStages * kStageBytes;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + (size_t)kWarpsPerCta * kStages * kStageBytes) +
+        wid * kStages;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // ---- issue side: next chunk to copy and a lane-parallel cache of row_index
+    int64_t ic = cb;
+    int64_t irow = cb / cpr;
+    int32_t ik = (int32_t)(cb - irow * cpr);
+    int64_t ri_base = -1;
+    int64_t ri_reg = 0;
+    auto src_row_of = [&](int64_t row) -> int64_t {   // warp-collective
+        if (p.row_index == nullptr) return row;
+        if (ri_base < 0 || row >= ri_base + 32 || row < ri_base) {
+            ri_base = row;
+            const int64_t rr = row + lane;
+            ri_reg = rr < p.n_rows ? __ldg(p.row_index + rr) : 0;
+        }
+        int64_t s = __shfl_sync(0xffffffffu, ri_reg, (int)(row - ri_base));
+        if (s < 0 || s >= p.n_logit_rows) s = 0;      // flagged on the consume side
+        return s;
+    };
+    auto issue_next = [&](int s) {                    // warp-collective
+        const int64_t srow = src_row_of(irow);
+        if (lane == 0) {
+            const uint32_t off = (uint32_t)ik * kStageBytes;
+            const uint32_t bytes = min((uint32_t)kStageBytes, (uint32_t)p.row_bytes - off);
+            const uint8_t *src = p.logits + srow * p.ld_bytes + off;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[s], bytes);
+            bulk_g2s(stage + (size_t)s * kStageBytes, src, bytes, &bars[s]);
+        }
+        ++ic;
+        if (++ik == cpr) {
+            ik = 0;
+            ++irow;
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+        if (ic < ce) issue_next(s);
+
+    // ---- consume side
+    int64_t row = cb / cpr;
+    int32_t k = (int32_t)(cb - row * cpr);
+    int64_t tb = -1;
+    int32_t tok_reg = 0;
+    int64_t rib_reg = 0;
+    int32_t tok = 0;
+    bool bad = false;
+    auto row_start = [&]() {                          // warp-collective
+        if (tb < 0 || row >= tb + 32) {
+            tb = row;
+            const int64_t rr = row + lane;
+            tok_reg = rr < p.n_rows ? __ldg(p.tokens + rr) : 0;
+            rib_reg = (p.row_index != nullptr && rr < p.n_rows) ? __ldg(p.row_index + rr) : 0;
+        }
+        tok = __shfl_sync(0xffffffffu, tok_reg, (int)(row - tb));
+        const int64_t src = __shfl_sync(0xffffffffu, rib_reg, (int)(row - tb));
+        const bool bad_tok = tok < 0 || tok >= p.V;
+        const bool bad_src = p.row_index != nullptr && (src < 0 || src >= p.n_logit_rows);
+        bad = bad_tok || bad_src;
+        if (lane == 0) {
+            if (bad_tok) set_status(p.status, PS_DEV_BAD_TOKEN);
+            if (bad_src) set_status(p.status, PS_DEV_BAD_ROW_INDEX);
+        }
+    };
+    row_start();
+
+    float R = -INFINITY, s1 = 0.f, st = 0.f;
+    float ltok = __uint_as_float(kAbsent);
+    uint32_t phase = 0;
+    int s = 0;                                        // stage of chunk c
+
+    for (int64_t c = cb; c < ce; ++c, s = (s + 1 == kStages) ? 0 : s + 1) {
+        if (!mbar_wait_bounded(&bars[s], (phase >> s) & 1u, kWaitLimitNs)) {
+            if (lane == 0) {
+                set_status(p.status, PS_DEV_TIMEOUT);
+                // let this warp's copies in flight land before the warp exits
+                for (int j = 0; j < kStages; ++j) {
+                    if (c + j < ic) {
+                        const int sj = (s + j) % kStages;
+                        mbar_wait_bounded(&bars[sj], (phase >> sj) & 1u, kDrainLimitNs);
+                    }
+                }
+            }
+            __syncwarp();
+            return;
+        }
+        phase ^= 1u << s;
+        uint8_t *buf = stage + (size_t)s * kStageBytes;
+        const uint32_t off = (uint32_t)k * kStageBytes;
+        const uint32_t bytes = min((uint32_t)kStageBytes, (uint32_t)p.row_bytes - off);
+        if (lane == 0) {
+            const int64_t e0 = (int64_t)k * kElemsPerStage;
+            const int64_t nel = bytes / kEsz;
+            if (!bad) {
+                const int64_t o = (int64_t)tok - e0;
+                if (o >= 0 && o < nel) {
+                    if constexpr (DT == PS_BF16) {
+                        uint16_t *h = reinterpret_cast<uint16_t *>(buf) + o;
+                        ltok = __uint_as_float((uint32_t)*h << 16);
+                        *h = 0xff80u;
+                    } else {
+                        float *f = reinterpret_cast<float *>(buf) + o;
+                        ltok = *f;
+                        *f = -INFINITY;
+                    }
+                }
+            }
+            if (k == cpr - 1) {
+                for (int64_t j = (int64_t)p.V - e0; j < nel; ++j) {
+                    if constexpr (DT == PS_BF16)
+                        reinterpret_cast<uint16_t *>(buf)[j] = 0xff80u;
+                    else
+                        reinterpret_cast<float *>(buf)[j] = -INFINITY;
+                }
+            }
+        }
+        __syncwarp();
+        {
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+            const int nvec = (int)(bytes >> 4);
+            uint4 q[kVecPerLane];
+            load_vecs<DT>(v4, nvec, lane, q);
+            float c1, ct;
+            sum_vecs<DT, NP>(q, R, g, c1, ct);
+            if (fmaxf(c1, ct) <= kLimit) {
+                s1 += c1;
+                if constexpr (NP != 1) st += ct;
+            } else {
+                const float3 r3 = slow_chunk<DT, NP>(v4, nvec, lane, g, R, s1, st);
+                R = r3.x;
+                s1 = r3.y;
+                st = r3.z;
+            }
+        }
+        __syncwarp();
+        if (ic < ce) issue_next(s);
+
+        const bool row_end = (k == cpr - 1) || (c == ce - 1);
+        if (row_end) {
+            if constexpr (NP == 1) st = s1;
+            warp_merge<NP>(R, s1, st, g);
+            const float lt = __shfl_sync(0xffffffffu, ltok, 0);
+            const int64_t rc0 = row * cpr, rc1 = rc0 + cpr;
+            if (rc0 >= cb && rc1 <= ce) {
+                if (lane == 0) finalize_row<NP>(p, row, R, s1, st, lt, bad);
+            } else {
+                const int64_t slot = (row == cb / cpr) ? 2 * vw : 2 * vw + 1;
+                const int64_t owner = warp_of_chunk(rc0, C, W);
+                const int64_t lastw = warp_of_chunk(rc1 - 1, C, W);
+                int last = 0;
+                if (lane == 0) {
+                    RowPart part;
+                    part.R = R;
+                    part.s1 = s1;
+                    part.st = st;
+                    part.ltok = lt;
+                    p.parts[slot] = part;
+                    __threadfence();
+                    const int old = atomicAdd(p.counters + owner, 1);
+                    last = (old == (int)(lastw - owner));
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    float Rm = -INFINITY, s1m = 0.f, stm = 0.f;
+                    float ltm = __uint_as_float(kAbsent);
+                    // lanes take the parts in warp order, then a fixed butterfly
+                    for (int64_t u = owner + lane; u <= lastw; u += 32) {
+                        const int64_t su = (row == range_begin(u, C, W) / cpr) ? 2 * u : 2 * u + 1;
+                        const float4 pv = __ldcg(reinterpret_cast<const float4 *>(p.parts + su));
+                        merge_part<NP>(Rm, s1m, stm, pv.x, pv.y, pv.z, g);
+                        if (__float_as_uint(pv.w) != kAbsent) ltm = pv.w;
+                    }
+                    warp_merge<NP>(Rm, s1m, stm, g);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float other = __shfl_xor_sync(0xffffffffu, ltm, o);
+                        if (__float_as_uint(ltm) == kAbsent) ltm = other;
+                    }
+                    if (lane == 0) {
+                        finalize_row<NP>(p, row, Rm, s1m, stm, ltm, bad);
+                        p.counters[owner] = 0;
+                    }
+                }
+            }
+            R = -INFINITY;
+            s1 = 0.f;
+            st = 0.f;
+            ltok = __uint_as_float(kAbsent);
+        }
+        if (++k == cpr) {
+            k = 0;
+            ++row;
+            if (c + 1 < ce) row_start();
+        }
+    }
+}
+
+template <int DT, int NP>
+cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
+    auto kern = score_rows_kernel<DT, NP>;
+    const size_t smem = score_rows_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<n_ctas, kWarpsPerCta * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
+    switch (p.npow) {
+        case 1: return launch_t<DT, 1>(p, n_ctas, stream);
+        case 2: return launch_t<DT, 2>(p, n_ctas, stream);
+        case 4: return launch_t<DT, 4>(p, n_ctas, stream);
+        case 8: return launch_t<DT, 8>(p, n_ctas, stream);
+        default: return launch_t<DT, 0>(p, n_ctas, stream);
+    }
+}
+
+}  // namespace
+
+size_t score_rows_smem_bytes() {
+    return (size_t)kWarpsPerCta * kStages * kStageBytes + (size_t)kWarpsPerCta * kStages * 8;
+}
+
+cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream) {
+    if (p.dtype == PS_BF16) return launch_dt<PS_BF16>(p, n_ctas, stream);
+    return launch_dt<PS_F32>(p, n_ctas, stream);
+}
+
+}  // namespace ps

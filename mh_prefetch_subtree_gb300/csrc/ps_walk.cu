@@ -1,0 +1,127 @@
+// K3: the MH walk over each chain's prefetched subtree (PreSTO section 3.2
+// step (3); Example 5; Algorithm 2, MHTransition).
+//
+// One warp per chain.  The warp first copies the chain's node arrays and its
+// requests' log A and uniforms into shared memory with coalesced loads (when
+// the chain fits), then lane 0 walks: at a node whose request was scored it
+// completes one transition, moving to the acceptance child when
+// log u <= log A and to the rejection child otherwise; it stops at a leaf, at
+// a node whose request was deferred, or after max_steps transitions.  The
+// walk is bounded by the chain's node count as well, so a cyclic tree cannot
+// loop; every id is range-checked and a bad one ends the walk with a status
+// bit.
+#include <math.h>
+
+#include "ps_internal.cuh"
+
+namespace ps {
+namespace {
+
+constexpr int kWalkWarps = 4;
+constexpr int kNodeCap = 512;   // nodes per chain held in shared memory
+constexpr int kSegCap = 256;    // segments per chain held in shared memory
+
+struct WalkSmem {
+    int32_t acc[kNodeCap];
+    int32_t rej[kNodeCap];
+    int32_t req[kNodeCap];
+    double la[kSegCap];
+    double u[kSegCap];
+};
+
+__global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams p) {
+    __shared__ WalkSmem sm[kWalkWarps];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int c = blockIdx.x * kWalkWarps + warp;
+    if (c >= p.n_chains) return;
+    const int stride = p.max_steps + 1;
+    int32_t *path = p.path ? p.path + (int64_t)c * stride : nullptr;
+
+    const int32_t n0 = p.chain_node0[c], n1 = p.chain_node0[c + 1];
+    const int32_t s0 = p.chain_seg0[c], s1 = p.chain_seg0[c + 1];
+    if (n0 < 0 || n1 > p.n_nodes || n1 <= n0 || s0 < 0 || s1 > p.n_seg || s1 <= s0) {
+        if (lane == 0) {
+            set_status(p.status, PS_DEV_BAD_TREE);
+            p.state_seg[c] = -1;
+            p.end_node[c] = -1;
+            p.k_delta[c] = 0;
+        }
+        if (path)
+            for (int i = lane; i < stride; i += 32) path[i] = -1;
+        return;
+    }
+    const int32_t nn = n1 - n0, ns = s1 - s0;
+    WalkSmem &w = sm[warp];
+    const bool staged = nn <= kNodeCap && ns <= kSegCap;
+    if (staged) {
+        for (int i = lane; i < nn; i += 32) {
+            w.acc[i] = p.acc[n0 + i];
+            w.rej[i] = p.rej[n0 + i];
+            w.req[i] = p.req[n0 + i];
+        }
+        for (int i = lane; i < ns; i += 32) {
+            w.la[i] = p.log_accept[s0 + i];
+            w.u[i] = p.u[s0 + i];
+        }
+    }
+    if (path)
+        for (int i = lane; i < stride; i += 32) path[i] = -1;
+    __syncwarp();
+    if (lane != 0) return;
+
+    auto ACC = [&](int32_t v) { return staged ? w.acc[v - n0] : p.acc[v]; };
+    auto REJ = [&](int32_t v) { return staged ? w.rej[v - n0] : p.rej[v]; };
+    auto REQ = [&](int32_t v) { return staged ? w.req[v - n0] : p.req[v]; };
+    auto LA = [&](int32_t s) { return staged ? w.la[s - s0] : p.log_accept[s]; };
+    auto U = [&](int32_t s) { return staged ? w.u[s - s0] : p.u[s]; };
+
+    int32_t v = n0;
+    int32_t state = s0;
+    int32_t k = 0;
+    int32_t bits = 0;
+    if (path) path[0] = v;
+    const int32_t bound = min(p.max_steps, nn);
+    while (k < bound) {
+        const int32_t s = REQ(v);
+        if (s == PS_NODE_LEAF || s == PS_NODE_DEFERRED) break;
+        if (s <= s0 || s >= s1) {          // not a request of this chain
+            bits |= PS_DEV_BAD_TREE;
+            break;
+        }
+        const double uu = U(s);
+        const double la = LA(s);
+        bool accept = false;
+        if (uu > 0.0 && uu <= 1.0) {
+            accept = log(uu) <= la;        // u <= A; a NaN log A rejects
+        } else {
+            bits |= PS_DEV_BAD_UNIFORM;
+        }
+        const int32_t nv = accept ? ACC(v) : REJ(v);
+        if (nv < n0 || nv >= n1) {
+            bits |= PS_DEV_BAD_TREE;
+            break;
+        }
+        ++k;
+        if (accept) state = s;
+        v = nv;
+        if (path) path[k] = v;
+    }
+    // more transitions than nodes can only come from a cycle
+    if (k == nn && k < p.max_steps && REQ(v) >= 0) bits |= PS_DEV_BAD_TREE;
+    if (bits) set_status(p.status, bits);
+    p.state_seg[c] = state;
+    p.end_node[c] = v;
+    p.k_delta[c] = k;
+}
+
+}  // namespace
+
+cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream) {
+    if (p.n_chains <= 0) return cudaSuccess;
+    const int grid = (p.n_chains + kWalkWarps - 1) / kWalkWarps;
+    walk_kernel<<<grid, kWalkWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ps

@@ -1,0 +1,161 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI,
+run the oracle on the same bytes, and compare with the stated tolerances.
+
+Tolerances (from the benchmark spec of the parity bar):
+  per-token log-probabilities: |gpu - oracle| <= 1e-4 |oracle| (+1e-300 so
+      that an exact 0 compares equal to -0);
+  log A: |gpu - oracle| <= 1e-3 absolute;
+  walk: path, end node, k_Delta and reached state identical, except after a
+      decision with |log u - log A| < 1e-3, where the GPU walk must still be
+      the walk its own log A values give.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mh_prefetch_subtree_gb300 as ps
+import oracle
+from tests.helpers import bf16_bits
+
+TOK_RTOL = 1e-4
+TOK_ATOL = 1e-300
+LA_ATOL = 1e-3
+NEAR_TIE = 1e-3
+
+
+def run_gpu(w, per_row: bool = True, sums: bool = True, stream=None) -> dict:
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
+                                row_index=w.row_index, per_row=per_row, sums=sums)
+    d.step(stream)
+    torch.cuda.synchronize()
+    out = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v)
+           for k, v in d.t.items()
+           if k in ("lp0", "lq", "lp_y", "lq_y", "lp_x", "lq_x", "log_ratio", "log_accept",
+                    "status", "wstatus", "state_seg", "end_node", "k_delta", "path")
+           and v is not None}
+    out["status"] = int(out["status"][0])
+    out["wstatus"] = int(out["wstatus"][0])
+    return out
+
+
+def oracle_rows(w, block_rows: int = 8192, threads: int | None = None):
+    """Per-row oracle values, copying logits to the host block by block."""
+    n = w.n_rows
+    lp0 = np.empty(n)
+    lq = np.empty(n)
+    toks = w.tokens.cpu().numpy()
+    if w.row_index is not None:
+        # rows come from a pool: score each pool row used once per token
+        ri = w.row_index.cpu().numpy()
+        key = ri.astype(np.int64) * (w.V + 1) + toks
+        uk, inv = np.unique(key, return_inverse=True)
+        pool_rows = (uk // (w.V + 1)).astype(np.int64)
+        pool_tok = (uk % (w.V + 1)).astype(np.int32)
+        a0 = np.empty(uk.shape[0])
+        aq = np.empty(uk.shape[0])
+        for i0 in range(0, uk.shape[0], block_rows):
+            i1 = min(uk.shape[0], i0 + block_rows)
+            idx = torch.from_numpy(pool_rows[i0:i1]).to(w.logits.device)
+            host = w.logits.index_select(0, idx)
+            lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
+            dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
+            a0[i0:i1], aq[i0:i1] = oracle.row_logprobs(lg, dt, w.V, pool_tok[i0:i1], w.tau,
+                                                       threads=threads)
+        return a0[inv], aq[inv]
+    for r0 in range(0, n, block_rows):
+        r1 = min(n, r0 + block_rows)
+        host = w.logits[r0:r1]
+        lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
+        dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
+        lp0[r0:r1], lq[r0:r1] = oracle.row_logprobs(lg, dt, w.V, toks[r0:r1], w.tau,
+                                                    threads=threads)
+    return lp0, lq
+
+
+def run_oracle(w, threads: int | None = None) -> dict:
+    lp0, lq = oracle_rows(w, threads=threads)
+    sums = oracle.suffix_sums(w.layout, lp0, lq)
+    r, la = oracle.log_accept(sums, w.alpha)
+    wk = oracle.walk(w.layout, la, w.u, w.max_steps)
+    out = dict(lp0=lp0, lq=lq, log_ratio=r, log_accept=la, walk=wk)
+    out.update(sums)
+    return out
+
+
+def check_rows(g: dict, o: dict, rtol: float = TOK_RTOL) -> dict:
+    stats = {}
+    for k in ("lp0", "lq"):
+        a, b = g[k], o[k]
+        assert a.shape == b.shape
+        assert np.array_equal(np.isnan(a), np.isnan(b)), f"{k}: NaN pattern differs"
+        m = ~np.isnan(b)
+        err = np.abs(a[m] - b[m])
+        bound = rtol * np.abs(b[m]) + TOK_ATOL
+        bad = np.nonzero(err > bound)[0]
+        assert bad.size == 0, (f"{k}: {bad.size} rows off; worst rel "
+                               f"{np.max(err / (np.abs(b[m]) + 1e-300)):.3e}")
+        rel = err / np.maximum(np.abs(b[m]), 1e-300)
+        stats[f"{k}_max_rel"] = float(rel.max()) if rel.size else 0.0
+    return stats
+
+
+def check_log_accept(w, g: dict, o: dict, atol: float = LA_ATOL) -> dict:
+    req = ~w.layout.is_root()
+    stats = {}
+    for k in ("log_accept", "log_ratio"):
+        a, b = g[k][req], o[k][req]
+        assert np.array_equal(np.isnan(a), np.isnan(b)), f"{k}: NaN pattern differs"
+        m = ~np.isnan(b)
+        err = np.abs(a[m] - b[m])
+        assert (err <= atol).all(), f"{k}: max |diff| {err.max():.3e}"
+        stats[f"{k}_max_abs"] = float(err.max()) if err.size else 0.0
+    for k in ("lp_y", "lq_y", "lp_x", "lq_x"):
+        if k in g:
+            a, b = g[k][req], o[k][req]
+            err = np.abs(a - b)
+            stats[f"{k}_max_abs"] = float(np.nanmax(err)) if err.size else 0.0
+    return stats
+
+
+def check_walk(w, g: dict, o: dict) -> dict:
+    """Walk parity with the near-tie rule."""
+    lay = w.layout
+    mine = oracle.walk(lay, g["log_accept"], w.u, w.max_steps)   # GPU log A, oracle walk
+    stride = w.max_steps + 1
+    near = 0
+    for c in range(lay.n_chains):
+        gp = g["path"][c * stride:(c + 1) * stride]
+        k = int(g["k_delta"][c])
+        gpath = list(gp[:k + 1])
+        assert all(x == -1 for x in gp[k + 1:])
+        # the GPU walk is the walk its own log A values give
+        assert gpath == mine["path"][c]
+        assert int(g["state_seg"][c]) == int(mine["state_seg"][c])
+        assert int(g["end_node"][c]) == int(mine["end_node"][c])
+        opath = o["walk"]["path"][c]
+        if gpath != opath:
+            i = next(j for j in range(min(len(gpath), len(opath))) if gpath[j] != opath[j])
+            s = int(lay.req[gpath[i - 1]])
+            gap = abs(np.log(w.u[s]) - o["log_accept"][s])
+            assert gap < NEAR_TIE, f"chain {c}: walks differ at a decision {gap:.3e} from a tie"
+            near += 1
+        else:
+            assert int(g["k_delta"][c]) == int(o["walk"]["k_delta"][c])
+            assert int(g["state_seg"][c]) == int(o["walk"]["state_seg"][c])
+    return dict(walk_near_ties=near, k_delta_mean=float(np.mean(g["k_delta"])))
+
+
+def full_parity(w, threads: int | None = None) -> dict:
+    g = run_gpu(w)
+    assert g["status"] == 0, ps.dev_status_names(g["status"])
+    assert g["wstatus"] == 0, ps.dev_status_names(g["wstatus"])
+    o = run_oracle(w, threads=threads)
+    stats = {}
+    stats.update(check_rows(g, o))
+    stats.update(check_log_accept(w, g, o))
+    stats.update(check_walk(w, g, o))
+    stats["eps_certain"] = oracle.eps_certain_fraction(o["log_accept"][~w.layout.is_root()])
+    return stats
