@@ -189,6 +189,36 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
                               const double *lq, const ps_score_out *out, void *cuda_stream);
 
 /*
+ * ps_score_subtree_noalloc: the same scoring as ps_score_subtree, for callers
+ * that cannot allocate device memory and so cannot provide a workspace.  The
+ * pages have no counterpart of this entry point; it exists for embedding.
+ * Examples of such callers: a sampler hook running inside another engine whose
+ * device memory is owned by that engine's pool, code executing in a region
+ * where a cudaMalloc would stall or is forbidden (it synchronises the device),
+ * or a host program that only receives device pointers from elsewhere.
+ *
+ * Instead of a caller workspace it uses one static device array compiled into
+ * libps (about 4.2 MB, held on every GPU that loads the library until the
+ * process exits).  It never calls cudaMalloc, cudaFree or any allocating
+ * routine.  Inputs and outputs are the caller's, exactly as in
+ * ps_score_subtree.
+ *
+ * Limit: when out->lp0 or out->lq is NULL, the per-row values are kept in the
+ * static array, which holds at most 262144 rows; a larger batch returns
+ * PS_ERR_WORKSPACE without launching anything.  With both lp0 and lq supplied
+ * there is no row limit.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.
+ * Sharing: every call uses the same array, which keeps the previous call's
+ * contents (the arrival counters are zeroed on the stream at each call).  Calls
+ * whose work overlaps on the GPU (different streams, or different host threads,
+ * without ordering between them) race on it and give wrong results; order them.
+ */
+ps_status ps_score_subtree_noalloc(const ps_subtree_batch *batch, const ps_score_out *out,
+                                   void *cuda_stream);
+
+/*
  * The prefetched subtree of every chain, for the walk (section 3.2 step (3)).
  * Node ids and segment ids are global (the same numbering as the batch).
  * chain_node0  [n_chains+1] CSR offsets into nodes; the first node of a chain

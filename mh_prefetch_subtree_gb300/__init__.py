@@ -92,6 +92,9 @@ def lib() -> ctypes.CDLL:
         L.ps_assemble_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp,
                                           ctypes.POINTER(PsScoreOut), _vp]
         L.ps_assemble_subtree.restype = ctypes.c_int
+        L.ps_score_subtree_noalloc.argtypes = [ctypes.POINTER(PsSubtreeBatch),
+                                               ctypes.POINTER(PsScoreOut), _vp]
+        L.ps_score_subtree_noalloc.restype = ctypes.c_int
         L.ps_walk_subtree.argtypes = [ctypes.POINTER(PsTree), _vp, ctypes.POINTER(PsWalkOut), _vp]
         L.ps_walk_subtree.restype = ctypes.c_int
         L.ps_validate_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsTree),
@@ -128,6 +131,18 @@ def ps_score_subtree(batch: PsSubtreeBatch, out: PsScoreOut, workspace: torch.Te
                                 _stream(stream, workspace))
     if check and st != PS_OK:
         raise PsError(st, "ps_score_subtree")
+    return st
+
+
+def ps_score_subtree_noalloc(batch: PsSubtreeBatch, out: PsScoreOut, stream=None,
+                             check: bool = True) -> int:
+    """Scoring for callers that cannot allocate device memory: no workspace
+    argument; libps uses its own static device array (see include/ps.h for the
+    row limit, the once-per-device set-up and why overlapping calls race)."""
+    st = lib().ps_score_subtree_noalloc(ctypes.byref(batch), ctypes.byref(out),
+                                        _stream(stream, None))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_score_subtree_noalloc")
     return st
 
 
@@ -191,9 +206,10 @@ def _ptr(x) -> int | None:
     raise TypeError(type(x))
 
 
-def _stream(stream, like: torch.Tensor):
+def _stream(stream, like: torch.Tensor | None):
     if stream is None:
-        return torch.cuda.current_stream(like.device).cuda_stream
+        dev = like.device if like is not None else None
+        return torch.cuda.current_stream(dev).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)

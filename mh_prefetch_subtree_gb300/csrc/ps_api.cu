@@ -379,3 +379,95 @@ ps_status ps_validate_subtree(const ps_subtree_batch *b, const ps_tree *t, char 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Scoring without a caller workspace: scratch lives in one static device array
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int64_t kNoAllocMaxRows = 262144;     // per-row values kept in the array
+constexpr int kNoAllocMaxWarps = 4096;           // split-row partials and counters
+constexpr size_t kNoAllocRowBytes = (size_t)kNoAllocMaxRows * 2 * sizeof(double);
+constexpr size_t kNoAllocPartBytes = (size_t)2 * kNoAllocMaxWarps * sizeof(ps::RowPart);
+constexpr size_t kNoAllocCntBytes = (size_t)kNoAllocMaxWarps * sizeof(int32_t);
+constexpr size_t kNoAllocBytes = kNoAllocRowBytes + kNoAllocPartBytes + kNoAllocCntBytes;
+}  // namespace
+
+// About 4.2 MB on every device that loads the library.  Host code must not use
+// this name as an address: it is a host-side stand-in; the device address comes
+// from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char ps_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+// Device address of ps_noalloc_scratch on device `dev` (which the caller has
+// made current); looked up once per device.
+ps_status noalloc_scratch(int dev, uint8_t **out) {
+    static std::mutex mu;
+    static std::vector<void *> addr;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)addr.size() <= dev) addr.resize(dev + 1, nullptr);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, ps_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return PS_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *out = (uint8_t *)addr[dev];
+    return PS_OK;
+}
+}  // namespace
+
+extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const ps_score_out *out,
+                                              void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    const bool rows_in_scratch = out->lp0 == nullptr || out->lq == nullptr;
+    if (rows_in_scratch && b->n_rows > kNoAllocMaxRows) return PS_ERR_WORKSPACE;
+    int sms = 0;
+    st = device_of(b->n_rows > 0 ? b->logits : out->log_accept, &sms);
+    if (st != PS_OK) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PS_ERR_CUDA;
+    uint8_t *base = nullptr;
+    st = noalloc_scratch(dev, &base);
+    if (st != PS_OK) return st;
+    cudaStream_t stream = (cudaStream_t)cuda_stream;
+    double *lp0 = rows_in_scratch ? (double *)base : out->lp0;
+    double *lq = rows_in_scratch ? (double *)base + kNoAllocMaxRows : out->lq;
+
+    if (b->n_rows > 0) {
+        const int esz = elem_size(b->dtype);
+        ps::RowsParams p;
+        p.logits = (const uint8_t *)b->logits;
+        p.ld_bytes = b->ld * esz;
+        p.n_logit_rows = b->row_index ? b->n_logit_rows : b->n_rows;
+        p.row_index = b->row_index;
+        p.tokens = b->tokens;
+        p.n_rows = b->n_rows;
+        p.V = b->V;
+        p.dtype = b->dtype;
+        p.row_bytes = (int32_t)(((int64_t)b->V * esz + 15) / 16 * 16);
+        p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
+        p.n_chunks = b->n_rows * p.cpr;
+        int64_t warps = (int64_t)sms * ps::kWarpsPerCta;
+        if (warps > kNoAllocMaxWarps) warps = kNoAllocMaxWarps;   // fits the array
+        if (warps > p.n_chunks) warps = p.n_chunks;
+        p.n_vwarps = (int32_t)warps;
+        p.npow = integer_power(b->tau);
+        p.g = (float)(1.0 / b->tau);
+        p.lp0 = lp0;
+        p.lq = lq;
+        p.parts = (ps::RowPart *)(base + kNoAllocRowBytes);
+        p.counters = (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes);
+        p.status = out->status;
+        const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
+        // the counters must start at zero: the array keeps the last call's contents
+        st = map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
+        if (st != PS_OK) return st;
+        st = map_cuda(ps::launch_score_rows(p, n_ctas, stream));
+        if (st != PS_OK) return st;
+    }
+    return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
+}
