@@ -136,9 +136,11 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in use)}
 
 
-def build_workload(config: int, dev, rank: int):
+def build_workload(config: int, dev, rank: int, n_pf=None):
     from synth import make_workload
     kw = {}
+    if n_pf is not None:
+        kw["n_pf"] = n_pf
     if rank:
         kw["seed"] = 10086 + config + 7919 * rank
     return make_workload(config, device=dev, **kw)
@@ -236,6 +238,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n-pf", type=int, default=None,
+                    help="override the request budget (smaller batches for profiling)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -253,7 +257,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = build_workload(args.config, dev, rank)
+    w = build_workload(args.config, dev, rank, args.n_pf)
     lay = w.layout
     d = ps.DeviceSubtree.create(layout=lay, u=w.u, logits=w.logits, tokens=w.tokens, V=w.V,
                                 alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,

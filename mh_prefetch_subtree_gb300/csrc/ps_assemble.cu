@@ -10,10 +10,11 @@
 // why two contiguous row ranges hold the whole x suffix.
 //   r_i = (LQ_x - LQ_y) + alpha (LP_y - LP_x),  log A_i = min{0, r_i}.
 //
-// One CTA per chain, one warp per request.  Each warp sums its ranges in
-// float64 with lanes striding over rows and a fixed butterfly, so results are
-// bit-reproducible.  Every index is checked before use; a failing request gets
-// NaN outputs and a status bit.
+// One CTA per segment (a chain root only writes NaN to its own entries).  The
+// threads stride over the rows in float64 and the block reduces in a fixed
+// order (warp butterfly, then warps in index order), so results are
+// bit-reproducible.  Every index is checked before use; a failing request
+// gets NaN outputs and a status bit.
 #include <math.h>
 
 #include "ps_internal.cuh"
@@ -22,6 +23,7 @@ namespace ps {
 namespace {
 
 constexpr int kAssembleThreads = 256;
+constexpr int kAssembleWarps = kAssembleThreads / 32;
 
 __device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
@@ -29,96 +31,121 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const AssembleParams p) {
-    const int c = blockIdx.x;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+// Chain holding segment s: the last c with chain_seg0[c] <= s.
+__device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
+    int lo = 0, hi = n_chains - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chain_seg0[mid] <= s) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
 
+__global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const AssembleParams p) {
+    __shared__ double red[4][kAssembleWarps];
+    __shared__ int32_t sh_bits;
+    const int32_t s = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+    const int c = chain_of(p.chain_seg0, p.n_chains, s);
     const int32_t s0 = p.chain_seg0[c];
     const int32_t s1 = p.chain_seg0[c + 1];
-    if (s0 < 0 || s1 > p.n_seg || s1 <= s0) {
-        if (threadIdx.x == 0) set_status(p.status, PS_DEV_BAD_LAYOUT);
+    if (s == s0) {                                   // a chain root
+        if (tid == 0) {
+            double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
+            for (int j = 0; j < 6; ++j)
+                if (outs[j]) outs[j][s] = qnan;
+        }
         return;
     }
     const int32_t T = p.T;
-    const int32_t rc = p.seg_cut[s0];
-    const int64_t r0 = p.seg_row0[s0];
-    const int64_t r1 = p.seg_row0[s0 + 1];
-    const bool root_ok = p.seg_src[s0] == -1 && rc >= 0 && rc <= T && r0 >= 0 &&
-                         r1 <= p.n_rows && r1 - r0 == (int64_t)(T - rc);
-
-    if (threadIdx.x == 0) {
-        if (!root_ok) set_status(p.status, PS_DEV_BAD_LAYOUT);
-        double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
-        for (int j = 0; j < 6; ++j)
-            if (outs[j]) outs[j][s0] = qnan;
-    }
-
-    for (int32_t s = s0 + 1 + warp; s < s1; s += nwarps) {
-        const int32_t cs = p.seg_cut[s];
-        const int32_t src = p.seg_src[s];
-        const int64_t y0 = p.seg_row0[s];
-        const int64_t y1 = p.seg_row0[s + 1];
-        int32_t bits = root_ok ? 0 : PS_DEV_BAD_LAYOUT;
+    int32_t bits = 0;
+    if (s0 < 0 || s1 > p.n_seg || s1 <= s0 || s < s0 || s >= s1) bits |= PS_DEV_BAD_LAYOUT;
+    int32_t rc = 0, cs = 0, src = s0, csrc = T;
+    int64_t r0 = 0, y0 = 0, y1 = 0, q0 = 0, q1 = 0;
+    if (bits == 0) {
+        rc = p.seg_cut[s0];
+        r0 = p.seg_row0[s0];
+        const int64_t r1 = p.seg_row0[s0 + 1];
+        if (p.seg_src[s0] != -1 || rc < 0 || rc > T || r0 < 0 || r1 > p.n_rows ||
+            r1 - r0 != (int64_t)(T - rc))
+            bits |= PS_DEV_BAD_LAYOUT;
+        cs = p.seg_cut[s];
+        src = p.seg_src[s];
+        y0 = p.seg_row0[s];
+        y1 = p.seg_row0[s + 1];
         if (cs < 0 || cs > T - 1 || y0 < 0 || y1 > p.n_rows || y1 - y0 != (int64_t)(T - cs))
             bits |= PS_DEV_BAD_LAYOUT;
         if (src != s0 && (src <= s0 || src >= s1 || src == s)) bits |= PS_DEV_BAD_LAYOUT;
-        int32_t csrc = T;
-        int64_t q0 = 0, q1 = 0;
-        if (bits == 0 && src != s0) {
-            csrc = p.seg_cut[src];
-            q0 = p.seg_row0[src];
-            q1 = p.seg_row0[src + 1];
-            if (csrc < 0 || csrc > T - 1 || q0 < 0 || q1 > p.n_rows ||
-                q1 - q0 != (int64_t)(T - csrc))
-                bits |= PS_DEV_BAD_LAYOUT;
-        }
-        if (bits == 0 && (cs > csrc || cs < rc)) bits |= PS_DEV_INFEASIBLE;
+    }
+    if (bits == 0 && src != s0) {
+        csrc = p.seg_cut[src];
+        q0 = p.seg_row0[src];
+        q1 = p.seg_row0[src + 1];
+        if (csrc < 0 || csrc > T - 1 || q0 < 0 || q1 > p.n_rows ||
+            q1 - q0 != (int64_t)(T - csrc))
+            bits |= PS_DEV_BAD_LAYOUT;
+    }
+    if (bits == 0 && (cs > csrc || cs < rc)) bits |= PS_DEV_INFEASIBLE;
 
-        double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
-        if (bits == 0) {
-            double a = 0.0, b = 0.0;
-            for (int64_t r = y0 + lane; r < y1; r += 32) {
-                a += p.lp0[r];
-                b += p.lq[r];
-            }
-            ly = warp_sum(a);
-            qy = warp_sum(b);
-            a = 0.0;
-            b = 0.0;
-            const int64_t x0 = r0 + (cs - rc), x1 = r0 + (csrc - rc);
-            for (int64_t r = x0 + lane; r < x1; r += 32) {
-                a += p.lp0[r];
-                b += p.lq[r];
-            }
-            for (int64_t r = q0 + lane; r < q1; r += 32) {
-                a += p.lp0[r];
-                b += p.lq[r];
-            }
-            lx = warp_sum(a);
-            qx = warp_sum(b);
+    double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
+    if (bits == 0) {                                 // uniform across the block
+        double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
+        for (int64_t r = y0 + tid; r < y1; r += kAssembleThreads) {
+            a += p.lp0[r];
+            b += p.lq[r];
         }
+        const int64_t x0 = r0 + (cs - rc), x1 = r0 + (csrc - rc);
+        for (int64_t r = x0 + tid; r < x1; r += kAssembleThreads) {
+            e += p.lp0[r];
+            f += p.lq[r];
+        }
+        for (int64_t r = q0 + tid; r < q1; r += kAssembleThreads) {
+            e += p.lp0[r];
+            f += p.lq[r];
+        }
+        a = warp_sum(a);
+        b = warp_sum(b);
+        e = warp_sum(e);
+        f = warp_sum(f);
         if (lane == 0) {
-            if (bits) set_status(p.status, bits);
-            const double r = (qx - qy) + p.alpha * (ly - lx);
-            const double la = (r != r) ? qnan : fmin(0.0, r);
-            if (p.lp_y) p.lp_y[s] = ly;
-            if (p.lq_y) p.lq_y[s] = qy;
-            if (p.lp_x) p.lp_x[s] = lx;
-            if (p.lq_x) p.lq_x[s] = qx;
-            if (p.log_ratio) p.log_ratio[s] = r;
-            p.log_accept[s] = la;
+            red[0][warp] = a;
+            red[1][warp] = b;
+            red[2][warp] = e;
+            red[3][warp] = f;
         }
+        __syncthreads();
+        if (tid == 0) {
+            ly = qy = lx = qx = 0.0;
+            for (int w = 0; w < kAssembleWarps; ++w) {
+                ly += red[0][w];
+                qy += red[1][w];
+                lx += red[2][w];
+                qx += red[3][w];
+            }
+        }
+    }
+    if (tid == 0) {
+        if (bits) set_status(p.status, bits);
+        const double r = (qx - qy) + p.alpha * (ly - lx);
+        const double la = (r != r) ? qnan : fmin(0.0, r);
+        if (p.lp_y) p.lp_y[s] = ly;
+        if (p.lq_y) p.lq_y[s] = qy;
+        if (p.lp_x) p.lp_x[s] = lx;
+        if (p.lq_x) p.lq_x[s] = qx;
+        if (p.log_ratio) p.log_ratio[s] = r;
+        p.log_accept[s] = la;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream) {
-    if (p.n_chains <= 0) return cudaSuccess;
-    assemble_kernel<<<p.n_chains, kAssembleThreads, 0, stream>>>(p);
+    if (p.n_seg <= 0 || p.n_chains <= 0) return cudaSuccess;
+    assemble_kernel<<<p.n_seg, kAssembleThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -13,9 +13,9 @@ namespace ps {
 // row chunks through a private ring of shared-memory stages filled by 1-D bulk
 // copies; see ps_score_rows.cu.
 // ---------------------------------------------------------------------------
-constexpr int kWarpsPerCta = 16;
-constexpr int kStages = 3;
-constexpr int kStageBytes = 4096;
+constexpr int kWarpsPerCta = 8;
+constexpr int kStages = 2;
+constexpr int kStageBytes = 8192;
 constexpr int kMaxCtas = 2048;                        // workspace sizing bound
 constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
 

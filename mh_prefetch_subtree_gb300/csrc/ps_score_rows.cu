@@ -42,8 +42,6 @@ constexpr float kLn2f = 0.6931471805599453f;
 constexpr float kLimit = 1.8446744073709552e19f;   // 2^64: largest chunk sum kept as is
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s for one bulk copy
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kVecPerStage = kStageBytes / 16;     // 256 x 16 B
-constexpr int kVecPerLane = kVecPerStage / 32;     // 8
 constexpr uint32_t kAbsent = 0x7fc0deadu;           // "token not in this part" (a NaN payload
                                                     // no bf16/f32 logit converts to)
 
@@ -95,9 +93,9 @@ __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2
     }
 }
 
-// Sums of one lane's 8 vectors relative to reference R.
-template <int DT, int NP>
-__device__ __forceinline__ void sum_vecs(const uint4 (&q)[kVecPerLane], float R, float g,
+// Sums of one lane's VPL vectors relative to reference R.
+template <int DT, int NP, int VPL>
+__device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g,
                                          float &c1, float &ct) {
     const float2 L2 = make_float2(kLog2e, kLog2e);
     const float2 nR2 = make_float2(-R, -R);
@@ -109,7 +107,7 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[kVecPerLane], float R,
         at[j] = make_float2(0.f, 0.f);
     }
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
         if constexpr (DT == PS_BF16) {
 #pragma unroll
@@ -144,13 +142,18 @@ __device__ __forceinline__ float tau_scale(float d, float g) {
     else return ex2(d * (float)NP);
 }
 
-// Load one lane's 8 vectors of a stage; vectors past the chunk read as -inf.
-template <int DT>
+// Load one lane's VPL vectors of a stage; vectors past the chunk read as -inf.
+template <int DT, int VPL>
 __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
-                                          uint4 (&q)[kVecPerLane]) {
+                                          uint4 (&q)[VPL]) {
+    if (nvec == VPL * 32) {                    // a full chunk: no predication
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) q[i] = v4[lane + 32 * i];
+        return;
+    }
     const uint32_t ni = Elem<DT>::kNegInfWord;
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const int idx = lane + 32 * i;
         q[i] = idx < nvec ? v4[idx] : make_uint4(ni, ni, ni, ni);
     }
@@ -160,15 +163,15 @@ __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
 // lane's first chunk of a row, whose reference is still -inf).  Re-reads the
 // lane's vectors from shared memory, raises R to their maximum, rescales the
 // running sums and adds the chunk.
-template <int DT, int NP>
+template <int DT, int NP, int VPL>
 __device__ __noinline__ float3 slow_chunk(const uint4 *v4, int nvec, int lane, float g, float R,
                                           float s1, float st) {
-    uint4 q[kVecPerLane];
-    load_vecs<DT>(v4, nvec, lane, q);
+    uint4 q[VPL];
+    load_vecs<DT, VPL>(v4, nvec, lane, q);
     float m = -INFINITY;
     bool nan_seen = false;
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -198,7 +201,7 @@ __device__ __noinline__ float3 slow_chunk(const uint4 *v4, int nvec, int lane, f
         R = Rn;
     }
     float c1, ct;
-    sum_vecs<DT, NP>(q, R, g, c1, ct);
+    sum_vecs<DT, NP, VPL>(q, R, g, c1, ct);
     s1 += c1;
     if constexpr (NP != 1) st += ct;
     return make_float3(R, s1, st);
@@ -267,9 +270,15 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, float R, float s1, 
     p.lq[r] = oq;
 }
 
-template <int DT, int NP>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 1) score_rows_kernel(const RowsParams p) {
+// WARPS warps per CTA, each with a ring of STAGES stages of SB bytes.
+template <int DT, int NP, int WARPS, int STAGES, int SB>
+__global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kWarpsPerCta = WARPS;
+    constexpr int kStages = STAGES;
+    constexpr int kStageBytes = SB;
+    constexpr int kVecPerLane = SB / 16 / 32;
+    static_assert(SB % 512 == 0, "a stage holds a whole number of 16-byte vectors per lane");
     constexpr int kEsz = Elem<DT>::kSize;
     constexpr int kElemsPerStage = kStageBytes / kEsz;
     const int lane = threadIdx.x & 31;
@@ -413,14 +422,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) score_rows_kernel(const 
             const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
             const int nvec = (int)(bytes >> 4);
             uint4 q[kVecPerLane];
-            load_vecs<DT>(v4, nvec, lane, q);
+            load_vecs<DT, kVecPerLane>(v4, nvec, lane, q);
             float c1, ct;
-            sum_vecs<DT, NP>(q, R, g, c1, ct);
+            sum_vecs<DT, NP, kVecPerLane>(q, R, g, c1, ct);
             if (fmaxf(c1, ct) <= kLimit) {
                 s1 += c1;
                 if constexpr (NP != 1) st += ct;
             } else {
-                const float3 r3 = slow_chunk<DT, NP>(v4, nvec, lane, g, R, s1, st);
+                const float3 r3 = slow_chunk<DT, NP, kVecPerLane>(v4, nvec, lane, g, R, s1, st);
                 R = r3.x;
                 s1 = r3.y;
                 st = r3.z;
@@ -490,10 +499,15 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) score_rows_kernel(const 
     }
 }
 
+template <int WARPS, int STAGES, int SB>
+constexpr size_t smem_bytes_for() {
+    return (size_t)WARPS * STAGES * SB + (size_t)WARPS * STAGES * 8;
+}
+
 template <int DT, int NP>
 cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    auto kern = score_rows_kernel<DT, NP>;
-    const size_t smem = score_rows_smem_bytes();
+    auto kern = score_rows_kernel<DT, NP, kWarpsPerCta, kStages, kStageBytes>;
+    const size_t smem = smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -514,9 +528,7 @@ cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
 
 }  // namespace
 
-size_t score_rows_smem_bytes() {
-    return (size_t)kWarpsPerCta * kStages * kStageBytes + (size_t)kWarpsPerCta * kStages * 8;
-}
+size_t score_rows_smem_bytes() { return smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>(); }
 
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream) {
     if (p.dtype == PS_BF16) return launch_dt<PS_BF16>(p, n_ctas, stream);

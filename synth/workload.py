@@ -41,7 +41,7 @@ CONFIGS = {
     4: dict(name="gemma-vocab V=262144 bf16 T=2048 Npf=32 peaked",
             V=262144, dtype="bf16", T=2048, n_pf=32, depth_cap=None, max_steps=100,
             alpha=4.0, tau=0.25, tree="bfs", n_chains=1,
-            logits=("dominant", dict(sigma=3.0, margin_mu=8.0, margin_sd=2.0))),
+            logits=("dominant", dict(sigma=4.5, margin_mu=8.0, margin_sd=2.0))),
 }
 
 # config 5: 256 independent chains per sweep point over these grids

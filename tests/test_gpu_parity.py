@@ -51,9 +51,12 @@ def test_config3_full():
 
 
 def test_config4_full():
+    # the peaked-logits configuration is calibrated (sigma_b = 4.5) so that 67-95%
+    # of the decisions are epsilon-certain (A <= 0.01 or A >= 0.99)
     w = make_workload(4, device=DEV)
     s = H.full_parity(w)
     _report("config4", s)
+    assert 0.67 <= s["eps_certain"] <= 0.95
 
 
 def test_config5_sweep_points():
