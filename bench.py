@@ -277,9 +277,8 @@ def main():
     st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
     assert st == 0, ps.dev_status_names(st)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k1a, k1b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -287,22 +286,26 @@ def main():
     torch.cuda.synchronize()
     clocks.mark(True)
     with torch.cuda.stream(stream):
+        # the timed steps: nothing is recorded between the kernels of a step, so
+        # each kernel's launch overlaps the tail of the one before it
         start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
+        for _ in range(args.steps):
             d.score_rows(stream)
-            ev[i][1].record(stream)
             d.assemble(stream)
             d.walk(stream)
         end.record(stream)
+        # the scoring kernel alone, back to back, for its roofline
+        k1a.record(stream)
+        for _ in range(args.steps):
+            d.score_rows(stream)
+        k1b.record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
     if ws > 1:
         torch.distributed.barrier()
     clocks.stop()
     total_ms = start.elapsed_time(end)
-    k1_ms = [a.elapsed_time(b) for a, b in ev]
-    k1_avg = sum(k1_ms) / len(k1_ms)
+    k1_avg = k1a.elapsed_time(k1b) / args.steps
     if ws > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -338,6 +341,8 @@ def main():
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
         "rows_per_s": rows * ws / (total_ms / 1e3 / args.steps),
         "gpu_launches": 3 * args.steps,
+        "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
+                                     "walk_kernel": 1},
         "clocks": clocks.summary(),
     }
     if e2e is not None:
@@ -351,9 +356,16 @@ def main():
     return 0
 
 
-def e2e_leg(ps, w, d, dev, stream, args, ws):
-    """Same metric through ps_score_subtree + ps_walk_subtree, with the batch's
-    inputs copied from pinned host memory and the results read back, every step."""
+def e2e_leg(ps, w, d, dev, stream, args, ws, chunks: int = 8):
+    """Same metric through the public API with the batch's inputs in pinned host
+    memory and its results read back, every step.
+
+    The host-to-device copies of the logits and tokens are split into row
+    chunks on a copy stream; ps_score_rows scores each chunk as soon as it has
+    landed (the per-row scores of a chunk are independent), then
+    ps_assemble_subtree and ps_walk_subtree run and log A and the walk's
+    results are copied back.
+    """
     lay = w.layout
     h = {}
     h["logits"] = torch.empty(w.logits.shape, dtype=w.logits.dtype, pin_memory=True)
@@ -367,15 +379,38 @@ def e2e_leg(ps, w, d, dev, stream, args, ws):
     h2d = (h["logits"].numel() * h["logits"].element_size() + h["tokens"].numel() * 4
            + sum(v.numel() * v.element_size() for v in hmeta.values()))
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    n = w.n_rows
+    bounds = [n * i // chunks for i in range(chunks + 1)]
+    subs = []
+    for i in range(chunks):
+        r0, r1 = bounds[i], bounds[i + 1]
+        if r1 == r0:
+            continue
+        b = ps.make_batch(V=w.V, T=lay.T, alpha=w.alpha, tau=w.tau,
+                          chain_seg0=d.t["chain_seg0"], seg_row0=d.t["seg_row0"],
+                          seg_cut=d.t["seg_cut"], seg_src=d.t["seg_src"],
+                          logits=w.logits[r0:r1], tokens=w.tokens[r0:r1], n_rows=r1 - r0)
+        subs.append((r0, r1, b, d.t["lp0"][r0:r1], d.t["lq"][r0:r1]))
+    copy = torch.cuda.Stream(device=dev)
+    landed = [torch.cuda.Event() for _ in subs]
+    start_ev = torch.cuda.Event()
 
     def step():
-        w.logits.copy_(h["logits"], non_blocking=True)
-        w.tokens.copy_(h["tokens"], non_blocking=True)
-        for k, v in meta.items():
-            v.copy_(hmeta[k], non_blocking=True)
+        start_ev.record(stream)
+        copy.wait_event(start_ev)
+        with torch.cuda.stream(copy):
+            for k, v in meta.items():
+                v.copy_(hmeta[k], non_blocking=True)
+            for (r0, r1, _, _, _), ev in zip(subs, landed):
+                w.logits[r0:r1].copy_(h["logits"][r0:r1], non_blocking=True)
+                w.tokens[r0:r1].copy_(h["tokens"][r0:r1], non_blocking=True)
+                ev.record(copy)
         d.t["status"].zero_()
         d.t["wstatus"].zero_()
-        d.score(stream)
+        for (r0, r1, b, lp0, lq), ev in zip(subs, landed):
+            stream.wait_event(ev)
+            ps.ps_score_rows(b, lp0, lq, d.t["status"], d.workspace, stream)
+        d.assemble(stream)
         d.walk(stream)
         for k, v in outs.items():
             hout[k].copy_(v, non_blocking=True)
@@ -384,13 +419,15 @@ def e2e_leg(ps, w, d, dev, stream, args, ws):
         for _ in range(3):
             step()
     torch.cuda.synchronize()
+    st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
+    assert st == 0, ps.dev_status_names(st)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = args.e2e_steps
+    n_steps = args.e2e_steps
     if ws > 1:
         torch.distributed.barrier()
     with torch.cuda.stream(stream):
         a.record(stream)
-        for _ in range(n):
+        for _ in range(n_steps):
             step()
         b.record(stream)
     torch.cuda.synchronize()
@@ -399,9 +436,10 @@ def e2e_leg(ps, w, d, dev, stream, args, ws):
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    v = lay.suffix_tokens() * ws / (ms / 1e3 / n)
+    v = lay.suffix_tokens() * ws / (ms / 1e3 / n_steps)
     return {"value": v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": ms / n}
+            "d2h_bytes_per_step": int(d2h), "steps": n_steps, "ms_per_step": ms / n_steps,
+            "h2d_GBps": h2d / (ms / 1e3 / n_steps) / 1e9, "row_chunks": len(subs)}
 
 
 if __name__ == "__main__":

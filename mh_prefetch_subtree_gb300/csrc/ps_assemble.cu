@@ -31,6 +31,41 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
+// Adds lp0[r], lq[r] for r = r0, r0 + 256, ... < r1 into a, b, in index order;
+// the loads of up to 8 rows are issued before any of them is added.
+__device__ __forceinline__ void range_sum(const double *lp0, const double *lq, int64_t r0,
+                                          int64_t r1, double &a, double &b) {
+    constexpr int kU = 8;
+    int64_t r = r0;
+    for (; r + (kU - 1) * kAssembleThreads < r1; r += kU * kAssembleThreads) {
+        double x[kU], y[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            x[j] = __ldcg(lp0 + r + j * kAssembleThreads);
+            y[j] = __ldcg(lq + r + j * kAssembleThreads);
+        }
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            a += x[j];
+            b += y[j];
+        }
+    }
+    double x[kU], y[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+        const int64_t rr = r + j * kAssembleThreads;
+        x[j] = rr < r1 ? __ldcg(lp0 + rr) : 0.0;
+        y[j] = rr < r1 ? __ldcg(lq + rr) : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+        if (r + j * kAssembleThreads < r1) {
+            a += x[j];
+            b += y[j];
+        }
+    }
+}
+
 // Chain holding segment s: the last c with chain_seg0[c] <= s.
 __device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
     int lo = 0, hi = n_chains - 1;
@@ -44,12 +79,12 @@ __device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
 
 __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const AssembleParams p) {
     __shared__ double red[4][kAssembleWarps];
-    __shared__ int32_t sh_bits;
     const int32_t s = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+    pdl_launch_dependents();                         // the walk may be scheduled now
     const int c = chain_of(p.chain_seg0, p.n_chains, s);
     const int32_t s0 = p.chain_seg0[c];
     const int32_t s1 = p.chain_seg0[c + 1];
@@ -92,21 +127,13 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     if (bits == 0 && (cs > csrc || cs < rc)) bits |= PS_DEV_INFEASIBLE;
 
     double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
+    pdl_wait_prerequisites();                        // per-row values are now visible
     if (bits == 0) {                                 // uniform across the block
         double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
-        for (int64_t r = y0 + tid; r < y1; r += kAssembleThreads) {
-            a += p.lp0[r];
-            b += p.lq[r];
-        }
+        range_sum(p.lp0, p.lq, y0 + tid, y1, a, b);
         const int64_t x0 = r0 + (cs - rc), x1 = r0 + (csrc - rc);
-        for (int64_t r = x0 + tid; r < x1; r += kAssembleThreads) {
-            e += p.lp0[r];
-            f += p.lq[r];
-        }
-        for (int64_t r = q0 + tid; r < q1; r += kAssembleThreads) {
-            e += p.lp0[r];
-            f += p.lq[r];
-        }
+        range_sum(p.lp0, p.lq, x0 + tid, x1, e, f);
+        range_sum(p.lp0, p.lq, q0 + tid, q1, e, f);
         a = warp_sum(a);
         b = warp_sum(b);
         e = warp_sum(e);
@@ -145,8 +172,17 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
 
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream) {
     if (p.n_seg <= 0 || p.n_chains <= 0) return cudaSuccess;
-    assemble_kernel<<<p.n_seg, kAssembleThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_seg);
+    cfg.blockDim = dim3(kAssembleThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, assemble_kernel, p);
 }
 
 }  // namespace ps

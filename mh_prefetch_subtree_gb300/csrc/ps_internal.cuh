@@ -81,7 +81,10 @@ struct WalkParams {
     int32_t *status;
 };
 
-// Launchers (host side, asynchronous on `stream`).
+// Launchers (host side, asynchronous on `stream`).  The assemble and walk
+// kernels are launched with programmatic stream serialization, so each may
+// start while its predecessor in the stream finishes; they wait
+// (griddepcontrol.wait) before reading anything that predecessor writes.
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream);
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);
@@ -146,14 +149,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// 1-D bulk copy global -> shared, completion counted on an mbarrier.
-// dst and src 16-byte aligned, bytes a multiple of 16.
+// L2 policy for data read exactly once: evict it first, so that the small
+// arrays the next kernels read stay cached.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier, with an
+// L2 cache policy.  dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
+                                         uint64_t *bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -162,6 +173,15 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now / wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {

@@ -22,8 +22,8 @@
 // ranges, one per warp, so every warp streams about the same number of bytes
 // whatever the row count.  Each warp owns a ring of 3 shared-memory stages that
 // its lane 0 fills with 1-D bulk copies (cp.async.bulk, completion on an
-// mbarrier); the warp consumes a stage, refills it, and moves on.  There is no
-// block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
+// mbarrier, L2 evict-first since every byte is read once); the warp consumes a
+// stage, refills it, and moves on.  There is no block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
 // row's token logit (after saving it) and any padding beyond V with -inf.
 //
 // A row whose chunks all lie in one warp's range is finalised by that warp.
@@ -283,6 +283,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
     constexpr int kElemsPerStage = kStageBytes / kEsz;
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
+    // the next kernel (suffix sums) may be scheduled now; it waits for this
+    // grid to complete before it reads the per-row results
+    pdl_launch_dependents();
     const int64_t W = p.n_vwarps;
     const int64_t vw = (int64_t)blockIdx.x * kWarpsPerCta + wid;
     if (vw >= W) return;
@@ -302,6 +305,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
         fence_mbar_init();
     }
     __syncwarp();
+
+    const uint64_t policy = l2_evict_first_policy();   // logits are read once
 
     // ---- issue side: next chunk to copy and a lane-parallel cache of row_index
     int64_t ic = cb;
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             const uint8_t *src = p.logits + srow * p.ld_bytes + off;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(stage + (size_t)s * kStageBytes, src, bytes, &bars[s]);
+            bulk_g2s(stage + (size_t)s * kStageBytes, src, bytes, &bars[s], policy);
         }
         ++ic;
         if (++ik == cpr) {

@@ -2,10 +2,11 @@
 // step (3); Example 5; Algorithm 2, MHTransition).
 //
 // One warp per chain.  The warp first copies the chain's node arrays and its
-// requests' log A and uniforms into shared memory with coalesced loads (when
-// the chain fits), then lane 0 walks: at a node whose request was scored it
-// completes one transition, moving to the acceptance child when
-// log u <= log A and to the rejection child otherwise; it stops at a leaf, at
+// requests' uniforms into shared memory with coalesced loads (when the chain
+// fits), the lanes take every request's accept/reject decision at once, then
+// lane 0 walks: at a node whose request was scored it completes one
+// transition, moving to the acceptance child when u <= A = exp(log A) and to
+// the rejection child otherwise; it stops at a leaf, at
 // a node whose request was deferred, or after max_steps transitions.  The
 // walk is bounded by the chain's node count as well, so a cyclic tree cannot
 // loop; every id is range-checked and a bad one ends the walk with a status
@@ -25,9 +26,27 @@ struct WalkSmem {
     int32_t acc[kNodeCap];
     int32_t rej[kNodeCap];
     int32_t req[kNodeCap];
-    double la[kSegCap];
+    int8_t acc_dec[kSegCap];    // decide(u, log A) of each request of the chain
     double u[kSegCap];
 };
+
+// The decision of Algorithm 1 line 7, u <= A with A = exp(log A): 1 accept,
+// 0 reject, -1 the uniform is outside (0, 1].  A float exponential settles it
+// unless u is within 1e-5 (relative) of A or A is below float range; then the
+// float64 exponential decides.  A NaN log A rejects.
+__device__ __forceinline__ int8_t decide(double u, double la) {
+    if (!(u > 0.0 && u <= 1.0)) return -1;
+    if (!(la == la)) return 0;
+    if (la >= 0.0) return 1;
+    if (la > -80.0) {
+        // expf is within 2 ulps; rounding la to float moves the exponent by at
+        // most 80 * 2^-24, so a is within 5e-6 of A (relative)
+        const double a = (double)expf((float)la);
+        if (u < a * (1.0 - 1e-5)) return 1;
+        if (u > a * (1.0 + 1e-5)) return 0;
+    }
+    return u <= exp(la) ? 1 : 0;
+}
 
 __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams p) {
     __shared__ WalkSmem sm[kWalkWarps];
@@ -60,10 +79,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
             w.rej[i] = p.rej[n0 + i];
             w.req[i] = p.req[n0 + i];
         }
-        for (int i = lane; i < ns; i += 32) {
-            w.la[i] = p.log_accept[s0 + i];
-            w.u[i] = p.u[s0 + i];
-        }
+        for (int i = lane; i < ns; i += 32) w.u[i] = p.u[s0 + i];
+    }
+    pdl_wait_prerequisites();          // log A from the scoring kernels is now visible
+    if (staged) {
+        // each request's decision, taken by all lanes at once so that the walk
+        // below only follows it
+        for (int i = lane; i < ns; i += 32)
+            w.acc_dec[i] = decide(w.u[i], __ldcg(p.log_accept + s0 + i));
     }
     if (path)
         for (int i = lane; i < stride; i += 32) path[i] = -1;
@@ -73,8 +96,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
     auto ACC = [&](int32_t v) { return staged ? w.acc[v - n0] : p.acc[v]; };
     auto REJ = [&](int32_t v) { return staged ? w.rej[v - n0] : p.rej[v]; };
     auto REQ = [&](int32_t v) { return staged ? w.req[v - n0] : p.req[v]; };
-    auto LA = [&](int32_t s) { return staged ? w.la[s - s0] : p.log_accept[s]; };
-    auto U = [&](int32_t s) { return staged ? w.u[s - s0] : p.u[s]; };
+    auto DECISION = [&](int32_t s) {
+        return staged ? w.acc_dec[s - s0] : decide(p.u[s], __ldcg(p.log_accept + s));
+    };
 
     int32_t v = n0;
     int32_t state = s0;
@@ -89,14 +113,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
             bits |= PS_DEV_BAD_TREE;
             break;
         }
-        const double uu = U(s);
-        const double la = LA(s);
-        bool accept = false;
-        if (uu > 0.0 && uu <= 1.0) {
-            accept = log(uu) <= la;        // u <= A; a NaN log A rejects
-        } else {
-            bits |= PS_DEV_BAD_UNIFORM;
-        }
+        const int8_t dec = DECISION(s);
+        const bool accept = dec == 1;
+        if (dec < 0) bits |= PS_DEV_BAD_UNIFORM;
         const int32_t nv = accept ? ACC(v) : REJ(v);
         if (nv < n0 || nv >= n1) {
             bits |= PS_DEV_BAD_TREE;
@@ -119,9 +138,17 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
 
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream) {
     if (p.n_chains <= 0) return cudaSuccess;
-    const int grid = (p.n_chains + kWalkWarps - 1) / kWalkWarps;
-    walk_kernel<<<grid, kWalkWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.n_chains + kWalkWarps - 1) / kWalkWarps));
+    cfg.blockDim = dim3(kWalkWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, walk_kernel, p);
 }
 
 }  // namespace ps
