@@ -39,8 +39,9 @@ UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
-# ncu capture (profiles/score_rows_config2_ncu.md), valid for this source hash.
-NCU_TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+# ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
+NCU_TRAFFIC = {"source_sha1": "2aa40774de59b34f755bd126f39f0420ec1845b8",
+               "bytes_per_launch": 4160403712 + 3733504}
 
 
 def log(*a):
