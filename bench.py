@@ -55,6 +55,27 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (a no-op without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: int, world_size: int, steps: int, max_ms: float) -> float:
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return units_per_rank_step * world_size * steps / (max_ms / 1e3)
+
+
+def rank_seed(config: int, rank: int):
+    """Seed of each rank's batch: rank 0 uses the configuration's own seed, the
+    others independent seeds, so the ranks score different batches."""
+    return None if rank == 0 else 10086 + config + 7919 * rank
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -142,8 +163,9 @@ def build_workload(config: int, dev, rank: int, n_pf=None):
     kw = {}
     if n_pf is not None:
         kw["n_pf"] = n_pf
-    if rank:
-        kw["seed"] = 10086 + config + 7919 * rank
+    seed = rank_seed(config, rank)
+    if seed is not None:
+        kw["seed"] = seed
     return make_workload(config, device=dev, **kw)
 
 
@@ -305,14 +327,10 @@ def main():
     if ws > 1:
         torch.distributed.barrier()
     clocks.stop()
-    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(start.elapsed_time(end), dev)
     k1_avg = k1a.elapsed_time(k1b) / args.steps
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = units_per_step * ws / (total_ms / 1e3 / args.steps)
+    value = whole_job_rate(units_per_step, ws, args.steps, total_ms)
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
@@ -340,7 +358,7 @@ def main():
                      "kernel": "score_rows_kernel", "kernel_ms": k1_avg,
                      "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
-        "rows_per_s": rows * ws / (total_ms / 1e3 / args.steps),
+        "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
                                      "walk_kernel": 1},
@@ -432,12 +450,8 @@ def e2e_leg(ps, w, d, dev, stream, args, ws, chunks: int = 8):
             step()
         b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    v = lay.suffix_tokens() * ws / (ms / 1e3 / n_steps)
+    ms = max_over_ranks(a.elapsed_time(b), dev)
+    v = whole_job_rate(lay.suffix_tokens(), ws, n_steps, ms)
     return {"value": v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n_steps, "ms_per_step": ms / n_steps,
             "h2d_GBps": h2d / (ms / 1e3 / n_steps) / 1e9, "row_chunks": len(subs)}

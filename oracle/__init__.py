@@ -24,7 +24,9 @@ Sampling" (arXiv 2610.13171) in float64, step by step and without shortcuts:
 * ``replay``            sequential PowerMH on explicit states with the same
                         uniforms (Proposition 1);
 * ``expected_transitions``  F_I(v0) = sum of reaching weights (Lemma 1, eq. (11)-(12));
-* ``eps_certain_fraction``  the share of epsilon-certain decisions (section 3.3).
+* ``eps_class``, ``eps_certain_fraction``  epsilon-certainty of each decision
+                        and their share (section 3.3);
+* entropy of p0 per row (``row_logprobs(..., entropy=True)``; Appendix D.3).
 
 Every function is pinned by the ``-m "not gpu"`` tests against closed forms,
 library routines, brute force or the pages' worked examples.
@@ -69,7 +71,7 @@ def lib():
         L.oracle_row_logprobs.argtypes = [
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,
-            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         L.oracle_row_logprobs.restype = None
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
@@ -83,8 +85,9 @@ def default_threads() -> int:
 
 def row_logprobs(logits: np.ndarray, dtype: str, V: int, tokens: np.ndarray,
                  tau: float, row_index: np.ndarray | None = None,
-                 threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
-    """Per-row (lp0, lq) in float64.
+                 threads: int | None = None, entropy: bool = False):
+    """Per-row (lp0, lq) in float64, and the entropy of p0 when entropy=True
+    (then a third array is returned).
 
     ``logits`` is a 2-D array [n_logit_rows, ld]: uint16 holding bf16 bit
     patterns (dtype "bf16") or float32 (dtype "f32").  Row r reads logits row
@@ -112,10 +115,14 @@ def row_logprobs(logits: np.ndarray, dtype: str, V: int, tokens: np.ndarray,
         assert logits.shape[0] >= n
     lp0 = np.empty(n, dtype=np.float64)
     lq = np.empty(n, dtype=np.float64)
+    ent = np.empty(n, dtype=np.float64) if entropy else None
     lib().oracle_row_logprobs(
         logits.ctypes.data, dcode, int(V), int(ld), int(n),
         None if ri is None else ri.ctypes.data, tokens.ctypes.data, float(tau),
-        lp0.ctypes.data, lq.ctypes.data, int(threads or default_threads()))
+        lp0.ctypes.data, lq.ctypes.data, None if ent is None else ent.ctypes.data,
+        int(threads or default_threads()))
+    if entropy:
+        return lp0, lq, ent
     return lp0, lq
 
 
@@ -335,6 +342,16 @@ def expected_transitions(layout, logA: np.ndarray, max_steps: int) -> np.ndarray
             stack.append((int(layout.acc[v]), R * A, d + 1))
             stack.append((int(layout.rej[v]), R * (1.0 - A), d + 1))
         out[c] = tot
+    return out
+
+
+def eps_class(logA: np.ndarray, eps: float = 0.01) -> np.ndarray:
+    """epsilon-certainty class of each decision (section 3.3): 0 = certain
+    reject (A <= eps), 2 = certain accept (A >= 1 - eps), 1 = uncertain;
+    -1 where log A is NaN (chain roots)."""
+    A = np.exp(logA)
+    out = np.where(A <= eps, 0, np.where(A >= 1.0 - eps, 2, 1)).astype(np.int8)
+    out[np.isnan(logA)] = -1
     return out
 
 

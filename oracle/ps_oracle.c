@@ -34,12 +34,40 @@ static double elem(const void *row, int dtype, int64_t j)
     return (double)f;
 }
 
+/*
+ * Full-vocabulary entropy of p0 = softmax(l) in nats (PreSTO Appendix D.3,
+ * the quantity (iii) of the patched sampler): H = -sum_j p_j log p_j, written
+ * with m = max_j l_j (first index j*), E = sum_{j != j*} exp(l_j - m) and
+ * Z = 1 + E as
+ *     H = log1p(E) - sum_{j != j*} exp(l_j - m) (l_j - m) / Z
+ * (the max term has l_j - m = 0).  Keeping the max term out of the sums keeps
+ * the result accurate when one token holds nearly all the mass.  A -inf
+ * logit has probability 0 and contributes nothing.
+ */
+static double row_entropy(const void *row, int dtype, int64_t V, double m, int64_t jstar)
+{
+    double e_sum = 0.0, a = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        if (j == jstar)
+            continue;
+        double d = elem(row, dtype, j) - m;
+        if (d == -INFINITY)
+            continue;
+        double e = exp(d);
+        e_sum += e;
+        a += e * d;
+    }
+    return log1p(e_sum) - a / (1.0 + e_sum);
+}
+
 static void one_row(const void *row, int dtype, int64_t V, int32_t tok, double tau,
-                    double *lp0, double *lq)
+                    double *lp0, double *lq, double *ent)
 {
     if (tok < 0 || (int64_t)tok >= V) {
         *lp0 = NAN;
         *lq = NAN;
+        if (ent)
+            *ent = NAN;
         return;
     }
     double m = -INFINITY;
@@ -49,6 +77,8 @@ static void one_row(const void *row, int dtype, int64_t V, int32_t tok, double t
         if (isnan(l)) {
             *lp0 = NAN;
             *lq = NAN;
+            if (ent)
+                *ent = NAN;
             return;
         }
         if (l > m) {
@@ -59,6 +89,8 @@ static void one_row(const void *row, int dtype, int64_t V, int32_t tok, double t
     if (jstar < 0) {            /* every logit is -inf */
         *lp0 = NAN;
         *lq = NAN;
+        if (ent)
+            *ent = NAN;
         return;
     }
     double e1 = 0.0, et = 0.0;
@@ -72,23 +104,26 @@ static void one_row(const void *row, int dtype, int64_t V, int32_t tok, double t
     double dt = elem(row, dtype, tok) - m;
     *lp0 = dt - log1p(e1);
     *lq = dt / tau - log1p(et);
+    if (ent)
+        *ent = row_entropy(row, dtype, V, m, jstar);
 }
 
 /*
  * Score n_rows rows.  Row r reads logits row row_index[r] (or r when row_index
- * is NULL), at byte offset row * ld * element size from `logits`.
+ * is NULL), at byte offset row * ld * element size from `logits`.  `entropy`
+ * may be NULL; otherwise it receives H of p0 for every row.
  */
 void oracle_row_logprobs(const void *logits, int dtype, int64_t V, int64_t ld,
                          int64_t n_rows, const int64_t *row_index,
                          const int32_t *tokens, double tau, double *lp0, double *lq,
-                         int n_threads)
+                         double *entropy, int n_threads)
 {
     const size_t esz = dtype == 0 ? 2 : 4;
 #pragma omp parallel for schedule(dynamic, 16) num_threads(n_threads > 0 ? n_threads : 1)
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t src = row_index ? row_index[r] : r;
         const char *row = (const char *)logits + (size_t)src * (size_t)ld * esz;
-        one_row(row, dtype, V, tokens[r], tau, &lp0[r], &lq[r]);
+        one_row(row, dtype, V, tokens[r], tau, &lp0[r], &lq[r], entropy ? &entropy[r] : 0);
     }
 }
 
