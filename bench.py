@@ -175,11 +175,10 @@ def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
     from tests.gpu_harness import oracle_rows   # block-wise host copies for the oracle
     threads = oracle.default_threads()
     lay = w.layout
-    # sample: the root and the first requests whose rows fit ~max_seconds
-    # of oracle work at ~0.5 G logits/s per 8 cores, then the full sums,
-    # log A and walk of those requests
+    # the whole batch: per-row log-probabilities (and entropy), the suffix
+    # sums over explicit states, log A and the walk
     t0 = time.time()
-    lp0, lq = oracle_rows(w, threads=threads)
+    lp0, lq, _ent = oracle_rows(w, threads=threads)
     sums = oracle.suffix_sums(lay, lp0, lq)
     _, la = oracle.log_accept(sums, w.alpha)
     oracle.walk(lay, la, w.u, w.max_steps)
@@ -302,6 +301,8 @@ def main():
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k1a, k1b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k1c, k1d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ent_rows = torch.empty(w.n_rows, dtype=torch.float64, device=dev)
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -322,6 +323,12 @@ def main():
         for _ in range(args.steps):
             d.score_rows(stream)
         k1b.record(stream)
+        # and its variant that also returns the entropy of p0 per row
+        k1c.record(stream)
+        for _ in range(args.steps):
+            ps.ps_score_rows(d.batch, d.t["lp0"], d.t["lq"], d.t["status"], d.workspace,
+                             stream, entropy=ent_rows)
+        k1d.record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
     if ws > 1:
@@ -329,6 +336,7 @@ def main():
     clocks.stop()
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
     k1_avg = k1a.elapsed_time(k1b) / args.steps
+    k1_ent_avg = k1c.elapsed_time(k1d) / args.steps
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(units_per_step, ws, args.steps, total_ms)
 
@@ -358,6 +366,8 @@ def main():
                      "kernel": "score_rows_kernel", "kernel_ms": k1_avg,
                      "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
+        "with_entropy": {"kernel_ms": k1_ent_avg,
+                         "logits_GBps": logits_bytes / (k1_ent_avg / 1e3) / 1e9},
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
@@ -428,7 +438,7 @@ def e2e_leg(ps, w, d, dev, stream, args, ws, chunks: int = 8):
         d.t["wstatus"].zero_()
         for (r0, r1, b, lp0, lq), ev in zip(subs, landed):
             stream.wait_event(ev)
-            ps.ps_score_rows(b, lp0, lq, d.t["status"], d.workspace, stream)
+            ps.ps_score_rows(b, lp0, lq, d.t["status"], d.workspace, stream)  # no entropy
         d.assemble(stream)
         d.walk(stream)
         for k, v in outs.items():

@@ -99,6 +99,8 @@ typedef enum { PS_BF16 = 0, PS_F32 = 1 } ps_dtype;
  *              same chain other than i (the chain root's id when the decision
  *              node holds the current state); c_i <= c_src (Condition 1).
  * alpha, tau   power exponent (finite) and proposal temperature (> 0).
+ * eps          epsilon of the epsilon-certainty classes (section 3.3), in
+ *              (0, 1/2); read only when ps_score_out.eps_class is requested.
  */
 typedef struct {
     int32_t V;
@@ -112,6 +114,7 @@ typedef struct {
     int64_t n_logit_rows;
     double alpha;
     double tau;
+    double eps;
     const int32_t *chain_seg0;
     const int64_t *seg_row0;
     const int32_t *seg_cut;
@@ -132,6 +135,11 @@ typedef struct {
  * log_ratio    [n_seg] optional: r_i = (lq_x - lq_y) + alpha (lp_y - lp_x).
  * log_accept   [n_seg] required: log A_i = min{0, r_i} (eq. (6)).
  * status       device int32 word, required; the caller zeroes it.
+ * entropy      [n_rows] optional: full-vocabulary entropy of p0 of every row,
+ *              in nats (Appendix D.3, quantity (iii)), from the same pass.
+ * eps_class    [n_seg] optional int8: 0 if A_i <= eps (epsilon-certain
+ *              reject), 2 if A_i >= 1 - eps (epsilon-certain accept), 1
+ *              otherwise; -1 for chain roots and NaN entries (section 3.3).
  */
 typedef struct {
     double *lp0;
@@ -143,6 +151,8 @@ typedef struct {
     double *log_ratio;
     double *log_accept;
     int32_t *status;
+    double *entropy;
+    int8_t *eps_class;
 } ps_score_out;
 
 /*
@@ -175,16 +185,18 @@ ps_status ps_score_subtree(const ps_subtree_batch *batch, const ps_score_out *ou
  * ps_score_rows: log p0 and log q_tau of every row's token (Appendix B.1;
  * Appendix D.3).  Reads only V, dtype, tau, n_rows, ld, n_logit_rows, logits,
  * row_index and tokens of the batch.  lp0, lq: [n_rows] device float64,
- * required.  status: device int32 word, required.  workspace as for
- * ps_score_subtree (its per-row area is unused here).
+ * required.  entropy: [n_rows] device float64 or NULL (then not computed).
+ * status: device int32 word, required.  workspace as for ps_score_subtree
+ * (its per-row area is unused here).
  *
  * ps_assemble_subtree: suffix sums and log A of every request from per-row
  * values lp0 / lq already computed for the batch's rows (eq. (6)).  Reads the
  * segment arrays, T, alpha and n_rows of the batch; out->lp0 and out->lq are
  * ignored.
  */
-ps_status ps_score_rows(const ps_subtree_batch *batch, double *lp0, double *lq, int32_t *status,
-                        void *workspace, size_t workspace_bytes, void *cuda_stream);
+ps_status ps_score_rows(const ps_subtree_batch *batch, double *lp0, double *lq, double *entropy,
+                        int32_t *status, void *workspace, size_t workspace_bytes,
+                        void *cuda_stream);
 ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
                               const double *lq, const ps_score_out *out, void *cuda_stream);
 
@@ -198,7 +210,7 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
  * or a host program that only receives device pointers from elsewhere.
  *
  * Instead of a caller workspace it uses one static device array compiled into
- * libps (about 4.2 MB, held on every GPU that loads the library until the
+ * libps (about 4.5 MB, held on every GPU that loads the library until the
  * process exits).  It never calls cudaMalloc, cudaFree or any allocating
  * routine.  Inputs and outputs are the caller's, exactly as in
  * ps_score_subtree.

@@ -44,13 +44,14 @@ class PsSubtreeBatch(ctypes.Structure):
                 ("reserved0", ctypes.c_int32), ("n_rows", ctypes.c_int64),
                 ("ld", ctypes.c_int64), ("n_logit_rows", ctypes.c_int64),
                 ("alpha", ctypes.c_double), ("tau", ctypes.c_double),
-                ("chain_seg0", _vp), ("seg_row0", _vp), ("seg_cut", _vp), ("seg_src", _vp),
+                ("eps", ctypes.c_double), ("chain_seg0", _vp), ("seg_row0", _vp), ("seg_cut", _vp), ("seg_src", _vp),
                 ("logits", _vp), ("row_index", _vp), ("tokens", _vp)]
 
 
 class PsScoreOut(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("lp0", "lq", "lp_y", "lq_y", "lp_x", "lq_x",
-                                   "log_ratio", "log_accept", "status")]
+                                   "log_ratio", "log_accept", "status", "entropy",
+                                   "eps_class")]
 
 
 class PsTree(ctypes.Structure):
@@ -86,7 +87,7 @@ def lib() -> ctypes.CDLL:
         L.ps_score_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsScoreOut),
                                        _vp, ctypes.c_size_t, _vp]
         L.ps_score_subtree.restype = ctypes.c_int
-        L.ps_score_rows.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp, _vp, _vp,
+        L.ps_score_rows.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
         L.ps_score_rows.restype = ctypes.c_int
         L.ps_assemble_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp,
@@ -148,13 +149,14 @@ def ps_score_subtree_noalloc(batch: PsSubtreeBatch, out: PsScoreOut, stream=None
 
 def ps_score_rows(batch: PsSubtreeBatch, lp0: torch.Tensor, lq: torch.Tensor,
                   status: torch.Tensor, workspace: torch.Tensor, stream=None,
-                  check: bool = True) -> int:
+                  check: bool = True, entropy: torch.Tensor | None = None) -> int:
     _need(lp0, torch.float64, "lp0")
     _need(lq, torch.float64, "lq")
+    _need(entropy, torch.float64, "entropy", optional=True)
     _need(status, torch.int32, "status")
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().ps_score_rows(ctypes.byref(batch), _ptr(lp0), _ptr(lq), _ptr(status),
-                             _ptr(workspace), ws_bytes, _stream(stream, workspace))
+    st = lib().ps_score_rows(ctypes.byref(batch), _ptr(lp0), _ptr(lq), _ptr(entropy),
+                             _ptr(status), _ptr(workspace), ws_bytes, _stream(stream, workspace))
     if check and st != PS_OK:
         raise PsError(st, "ps_score_rows")
     return st
@@ -215,7 +217,8 @@ def _stream(stream, like: torch.Tensor | None):
     return int(stream)
 
 
-_NP_OF = {torch.int32: np.int32, torch.int64: np.int64, torch.float64: np.float64}
+_NP_OF = {torch.int32: np.int32, torch.int64: np.int64, torch.float64: np.float64,
+          torch.int8: np.int8}
 
 
 def _need(x, dtype: torch.dtype, name: str, optional: bool = False):
@@ -236,7 +239,7 @@ def _need(x, dtype: torch.dtype, name: str, optional: bool = False):
 def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0, seg_cut,
                seg_src, logits=None, tokens=None, row_index=None, n_rows: int | None = None,
                n_logit_rows: int | None = None, ld: int | None = None,
-               dtype: int | None = None) -> PsSubtreeBatch:
+               dtype: int | None = None, eps: float = 0.01) -> PsSubtreeBatch:
     """Fill a ps_subtree_batch from tensors (device for scoring, host for validation)."""
     _need(chain_seg0, torch.int32, "chain_seg0")
     _need(seg_row0, torch.int64, "seg_row0")
@@ -270,7 +273,7 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
         ld = -(-int(V) // per16) * per16
     b.ld = int(ld)
     b.n_logit_rows = int(0 if n_logit_rows is None else n_logit_rows)
-    b.alpha, b.tau = float(alpha), float(tau)
+    b.alpha, b.tau, b.eps = float(alpha), float(tau), float(eps)
     b.chain_seg0, b.seg_row0 = _ptr(chain_seg0), _ptr(seg_row0)
     b.seg_cut, b.seg_src = _ptr(seg_cut), _ptr(seg_src)
     b.logits, b.row_index, b.tokens = _ptr(logits), _ptr(row_index), _ptr(tokens)
@@ -279,15 +282,19 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
 
 
 def make_score_out(*, log_accept, status, lp0=None, lq=None, lp_y=None, lq_y=None, lp_x=None,
-                   lq_x=None, log_ratio=None) -> PsScoreOut:
+                   lq_x=None, log_ratio=None, entropy=None, eps_class=None) -> PsScoreOut:
     o = PsScoreOut()
     for name, x in (("lp0", lp0), ("lq", lq), ("lp_y", lp_y), ("lq_y", lq_y), ("lp_x", lp_x),
-                    ("lq_x", lq_x), ("log_ratio", log_ratio), ("log_accept", log_accept)):
+                    ("lq_x", lq_x), ("log_ratio", log_ratio), ("log_accept", log_accept),
+                    ("entropy", entropy)):
         _need(x, torch.float64, name, optional=name != "log_accept")
         setattr(o, name, _ptr(x))
     _need(status, torch.int32, "status")
+    _need(eps_class, torch.int8, "eps_class", optional=True)
     o.status = _ptr(status)
-    o._keep = (lp0, lq, lp_y, lq_y, lp_x, lq_x, log_ratio, log_accept, status)
+    o.eps_class = _ptr(eps_class)
+    o._keep = (lp0, lq, lp_y, lq_y, lp_x, lq_x, log_ratio, log_accept, status, entropy,
+               eps_class)
     return o
 
 
@@ -342,7 +349,8 @@ class DeviceSubtree:
     @classmethod
     def create(cls, *, layout, u, logits: torch.Tensor, tokens: torch.Tensor, V: int,
                alpha: float, tau: float, max_steps: int, row_index: torch.Tensor | None = None,
-               per_row: bool = True, sums: bool = True, path: bool = True) -> "DeviceSubtree":
+               per_row: bool = True, sums: bool = True, path: bool = True,
+               entropy: bool = False, eps: float | None = None) -> "DeviceSubtree":
         dev = logits.device
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
         t = dict(
@@ -363,6 +371,9 @@ class DeviceSubtree:
         for k in ("lp_y", "lq_y", "lp_x", "lq_x", "log_ratio"):
             t[k] = f64(n_seg) if sums else None
         t["log_accept"] = f64(n_seg)
+        t["entropy"] = f64(n_rows) if entropy else None
+        t["eps_class"] = (torch.empty(n_seg, dtype=torch.int8, device=dev)
+                          if eps is not None else None)
         t["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
         t["wstatus"] = torch.zeros(1, dtype=torch.int32, device=dev)
         for k in ("state_seg", "end_node", "k_delta"):
@@ -371,12 +382,14 @@ class DeviceSubtree:
                      if path else None)
         batch = make_batch(V=V, T=layout.T, alpha=alpha, tau=tau, chain_seg0=t["chain_seg0"],
                            seg_row0=t["seg_row0"], seg_cut=t["seg_cut"], seg_src=t["seg_src"],
-                           logits=logits, tokens=tokens, row_index=row_index, n_rows=n_rows)
+                           logits=logits, tokens=tokens, row_index=row_index, n_rows=n_rows,
+                           eps=0.01 if eps is None else eps)
         ws_bytes = ps_score_workspace_bytes(batch)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         sout = make_score_out(log_accept=t["log_accept"], status=t["status"], lp0=t["lp0"],
                               lq=t["lq"], lp_y=t["lp_y"], lq_y=t["lq_y"], lp_x=t["lp_x"],
-                              lq_x=t["lq_x"], log_ratio=t["log_ratio"])
+                              lq_x=t["lq_x"], log_ratio=t["log_ratio"], entropy=t["entropy"],
+                              eps_class=t["eps_class"])
         tree = make_tree(chain_node0=t["chain_node0"], chain_seg0=t["chain_seg0"], acc=t["acc"],
                          rej=t["rej"], req=t["req"], u=t["u"], max_steps=max_steps)
         wout = make_walk_out(state_seg=t["state_seg"], end_node=t["end_node"],
@@ -389,7 +402,7 @@ class DeviceSubtree:
     def score_rows(self, stream=None) -> None:
         """First half of score(): per-row log-probabilities into t['lp0'], t['lq']."""
         ps_score_rows(self.batch, self.t["lp0"], self.t["lq"], self.t["status"],
-                      self.workspace, stream)
+                      self.workspace, stream, entropy=self.t["entropy"])
 
     def assemble(self, stream=None) -> None:
         """Second half of score(): suffix sums and log A from t['lp0'], t['lq']."""

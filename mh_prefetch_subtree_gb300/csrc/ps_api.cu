@@ -127,8 +127,9 @@ size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
     return ws_layout(batch->n_rows).total;
 }
 
-ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, int32_t *status,
-                        void *workspace, size_t workspace_bytes, void *cuda_stream) {
+ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, double *entropy,
+                        int32_t *status, void *workspace, size_t workspace_bytes,
+                        void *cuda_stream) {
     ps_status st = check_batch_host(b);
     if (st != PS_OK) return st;
     if (!lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
@@ -162,6 +163,7 @@ ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, int3
     p.g = (float)(1.0 / b->tau);
     p.lp0 = lp0;
     p.lq = lq;
+    p.entropy = entropy;
     p.parts = (ps::RowPart *)(ws + wl.parts_off);
     p.counters = (int32_t *)(ws + wl.cnt_off);
     p.status = status;
@@ -179,6 +181,7 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
     if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
     if (b->n_rows > 0 && (!lp0 || !lq)) return PS_ERR_INVALID_ARG;
+    if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
     int sms = 0;
     ps_status st = device_of(out->log_accept, &sms);
     if (st != PS_OK) return st;
@@ -200,6 +203,8 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     a.lq_x = out->lq_x;
     a.log_ratio = out->log_ratio;
     a.log_accept = out->log_accept;
+    a.eps = b->eps;
+    a.eps_class = out->eps_class;
     a.status = out->status;
     return map_cuda(ps::launch_assemble(a, (cudaStream_t)cuda_stream));
 }
@@ -215,7 +220,9 @@ ps_status ps_score_subtree(const ps_subtree_batch *b, const ps_score_out *out, v
     uint8_t *ws = (uint8_t *)workspace;
     double *lp0 = out->lp0 ? out->lp0 : (double *)(ws + wl.rows_off);
     double *lq = out->lq ? out->lq : (double *)(ws + wl.rows_off) + b->n_rows;
-    st = ps_score_rows(b, lp0, lq, out->status, workspace, workspace_bytes, cuda_stream);
+    if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
+    st = ps_score_rows(b, lp0, lq, out->entropy, out->status, workspace, workspace_bytes,
+                       cuda_stream);
     if (st != PS_OK) return st;
     return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
 }
@@ -392,7 +399,7 @@ constexpr size_t kNoAllocCntBytes = (size_t)kNoAllocMaxWarps * sizeof(int32_t);
 constexpr size_t kNoAllocBytes = kNoAllocRowBytes + kNoAllocPartBytes + kNoAllocCntBytes;
 }  // namespace
 
-// About 4.2 MB on every device that loads the library.  Host code must not use
+// About 4.5 MB on every device that loads the library.  Host code must not use
 // this name as an address: it is a host-side stand-in; the device address comes
 // from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char ps_noalloc_scratch[kNoAllocBytes];
@@ -423,6 +430,7 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     ps_status st = check_batch_host(b);
     if (st != PS_OK) return st;
     if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
     const bool rows_in_scratch = out->lp0 == nullptr || out->lq == nullptr;
     if (rows_in_scratch && b->n_rows > kNoAllocMaxRows) return PS_ERR_WORKSPACE;
     int sms = 0;
@@ -459,6 +467,7 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
         p.g = (float)(1.0 / b->tau);
         p.lp0 = lp0;
         p.lq = lq;
+        p.entropy = out->entropy;
         p.parts = (ps::RowPart *)(base + kNoAllocRowBytes);
         p.counters = (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes);
         p.status = out->status;

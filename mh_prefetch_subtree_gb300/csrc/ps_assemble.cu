@@ -8,7 +8,8 @@
 //          (c_src = T and no src rows when src is the root).
 // Condition 1 makes every state of the subtree x_{0:c_last} + y^last, which is
 // why two contiguous row ranges hold the whole x suffix.
-//   r_i = (LQ_x - LQ_y) + alpha (LP_y - LP_x),  log A_i = min{0, r_i}.
+//   r_i = (LQ_x - LQ_y) + alpha (LP_y - LP_x),  log A_i = min{0, r_i},
+// and, when asked, the epsilon-certainty class of the decision (section 3.3).
 //
 // One CTA per segment (a chain root only writes NaN to its own entries).  The
 // threads stride over the rows in float64 and the block reduces in a fixed
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
             double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
             for (int j = 0; j < 6; ++j)
                 if (outs[j]) outs[j][s] = qnan;
+            if (p.eps_class) p.eps_class[s] = -1;
         }
         return;
     }
@@ -165,6 +167,13 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
         if (p.lq_x) p.lq_x[s] = qx;
         if (p.log_ratio) p.log_ratio[s] = r;
         p.log_accept[s] = la;
+        if (p.eps_class) {
+            // epsilon-certainty (section 3.3), compared in the log domain:
+            // A <= eps  <=>  log A <= log eps;  A >= 1 - eps  <=>  log A >= log1p(-eps)
+            int8_t cls = -1;
+            if (la == la) cls = la <= log(p.eps) ? 0 : (la >= log1p(-p.eps) ? 2 : 1);
+            p.eps_class[s] = cls;
+        }
     }
 }
 

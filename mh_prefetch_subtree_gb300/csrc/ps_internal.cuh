@@ -19,14 +19,16 @@ constexpr int kStageBytes = 8192;
 constexpr int kMaxCtas = 2048;                        // workspace sizing bound
 constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
 
-// Partial log-sum-exp state of (part of) a row: sums of 2^(l*log2e - R) and
-// 2^(g*(l*log2e - R)) over the row's elements except the token, plus the
-// token's logit when this part held it (NaN otherwise).
+// Partial log-sum-exp state of (part of) a row: with y = l*log2e - R, the
+// sums of 2^y, 2^(g*y) and 2^y * y over the row's elements except the token,
+// plus the token's logit when this part held it (a marker NaN otherwise).
 struct __align__(16) RowPart {
     float R;
     float s1;
     float st;
     float ltok;
+    float y1;
+    float pad[3];
 };
 
 struct RowsParams {
@@ -46,6 +48,7 @@ struct RowsParams {
     float g;                    // 1/tau in float
     double *lp0;
     double *lq;
+    double *entropy;            // optional: entropy of p0 per row
     RowPart *parts;             // [2 * kMaxWarps]
     int32_t *counters;          // [kMaxWarps]
     int32_t *status;
@@ -57,6 +60,7 @@ struct AssembleParams {
     int32_t n_seg;
     int64_t n_rows;
     double alpha;
+    double eps;
     const int32_t *chain_seg0;
     const int64_t *seg_row0;
     const int32_t *seg_cut;
@@ -64,6 +68,7 @@ struct AssembleParams {
     const double *lp0;
     const double *lq;
     double *lp_y, *lq_y, *lp_x, *lq_x, *log_ratio, *log_accept;
+    int8_t *eps_class;
     int32_t *status;
 };
 

@@ -1,15 +1,17 @@
 // K1: per-token log p0 and log q_tau of every scored row, in one pass over
 // the row's logits (PreSTO, Appendix B.1 last paragraph and Appendix D.3:
 // both log-probabilities come from the same logits, without and with the
-// temperature).
+// temperature), and optionally the full-vocabulary entropy of p0 (Appendix
+// D.3, quantity (iii)) from the same pass.
 //
 // Formulation.  For a row l_0..l_{V-1} with token k, and any reference R
-// (log2 units), with L = log2(e) and g = 1/tau:
-//     S1 = sum_{j != k} 2^(l_j L - R),   St = sum_{j != k} 2^(g (l_j L - R)),
-//     t  = l_k L - R,
-//     log p0(k)    = -ln(1 + S1 2^-t),  log q_tau(k) = -ln(1 + St 2^(-g t)).
+// (log2 units), with L = log2(e), g = 1/tau and y_j = l_j L - R:
+//     S1 = sum_{j != k} 2^y_j,   St = sum_{j != k} 2^(g y_j),
+//     Y1 = sum_{j != k} 2^y_j y_j  (entropy only),   t = l_k L - R,
+//     log p0(k)    = -ln(1 + S1 2^-t),  log q_tau(k) = -ln(1 + St 2^(-g t)),
+//     H(p0)        = ln 2 (log2 Z - (Y1 + t 2^t) / Z),  Z = S1 + 2^t.
 // This is log softmax written relative to the token itself, so the token is
-// left out of both sums and the result keeps its relative accuracy when the
+// left out of the sums and the result keeps its relative accuracy when the
 // token holds nearly all the mass (the sums are then tiny, never 1 + tiny).
 // No maximum is needed: R only has to keep the exponentials in range.  Each
 // lane starts with R = -inf; a chunk whose sums overflow (or are NaN) takes a
@@ -17,13 +19,14 @@
 // 1, 2, 4 or 8 the tau exponential is the first one squared, so each logit
 // costs one MUFU ex2.
 //
-// Data movement.  The rows are cut into 4 KB chunks (the last chunk of a row
-// may be shorter).  The chunk sequence of all rows is split into contiguous
-// ranges, one per warp, so every warp streams about the same number of bytes
-// whatever the row count.  Each warp owns a ring of 3 shared-memory stages that
-// its lane 0 fills with 1-D bulk copies (cp.async.bulk, completion on an
-// mbarrier, L2 evict-first since every byte is read once); the warp consumes a
-// stage, refills it, and moves on.  There is no block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
+// Data movement.  The rows are cut into chunks of one stage (the last chunk of
+// a row may be shorter).  The chunk sequence of all rows is split into
+// contiguous ranges, one per warp, so every warp streams about the same number
+// of bytes whatever the row count.  Each warp owns a ring of shared-memory
+// stages that its lane 0 fills with 1-D bulk copies (cp.async.bulk,
+// completion on an mbarrier, L2 evict-first since every byte is read once);
+// the warp consumes a stage, refills it, and moves on.  There is no
+// block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
 // row's token logit (after saving it) and any padding beyond V with -inf.
 //
 // A row whose chunks all lie in one warp's range is finalised by that warp.
@@ -44,6 +47,11 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s for one bulk copy
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr uint32_t kAbsent = 0x7fc0deadu;           // "token not in this part" (a NaN payload
                                                     // no bf16/f32 logit converts to)
+// Entropy variant: logits below -1e30 (that is, -inf) are raised to -1e30, so
+// that 2^y * y is 0 * (finite) = 0 instead of 0 * (-inf) = NaN.  The exponential
+// of such a value is 0 either way; NaN is kept (the max propagates it).
+constexpr uint32_t kFloorBf16x2 = 0xf14af14au;      // (-1.0009e30, -1.0009e30) as bf16x2
+constexpr float kFloorF32 = -1.0e30f;
 
 __device__ __forceinline__ int64_t range_begin(int64_t w, int64_t C, int64_t W) {
     return (w * C) / W;
@@ -71,13 +79,36 @@ struct Elem<PS_F32> {
     static constexpr uint32_t kNegInfWord = 0xff800000u;
 };
 
-// One pair of logits: accumulate 2^(x) into a1 and 2^(g x) into at.
-template <int NP>
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Running sums of one lane (or one merged part) relative to reference R.
+struct Acc {
+    float R;
+    float s1;
+    float st;
+    float y1;
+};
+
+__device__ __forceinline__ Acc acc_empty() { return Acc{-INFINITY, 0.f, 0.f, 0.f}; }
+
+// One pair of logits: accumulate 2^x into a1, 2^(g x) into at and 2^x x into ay.
+template <int NP, bool ENT>
 __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2, float2 &a1,
-                                      float2 &at) {
+                                      float2 &at, float2 &ay) {
     const float2 x = __ffma2_rn(v, L2, nR2);
     const float2 e = make_float2(ex2(x.x), ex2(x.y));
     a1 = __fadd2_rn(a1, e);
+    if constexpr (ENT) ay = __ffma2_rn(e, x, ay);
     if constexpr (NP == 2) {
         at = __fadd2_rn(at, __fmul2_rn(e, e));
     } else if constexpr (NP == 4) {
@@ -94,33 +125,41 @@ __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2
 }
 
 // Sums of one lane's VPL vectors relative to reference R.
-template <int DT, int NP, int VPL>
-__device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g,
-                                         float &c1, float &ct) {
+template <int DT, int NP, bool ENT, int VPL>
+__device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g, float &c1,
+                                         float &ct, float &cy) {
     const float2 L2 = make_float2(kLog2e, kLog2e);
     const float2 nR2 = make_float2(-R, -R);
     const float2 G2 = make_float2(g, g);
-    float2 a1[4], at[4];
+    float2 a1[4], at[4], ay[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         a1[j] = make_float2(0.f, 0.f);
         at[j] = make_float2(0.f, 0.f);
+        ay[j] = make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-        const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+        uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
         if constexpr (DT == PS_BF16) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                if constexpr (ENT) w[j] = max_nan_bf16x2(w[j], kFloorBf16x2);
                 const float2 v = make_float2(__uint_as_float(w[j] << 16),
                                              __uint_as_float(w[j] & 0xffff0000u));
-                step2<NP>(v, L2, nR2, G2, a1[j], at[j]);
+                step2<NP, ENT>(v, L2, nR2, G2, a1[j], at[j], ay[j]);
             }
         } else {
-            step2<NP>(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])), L2, nR2, G2,
-                      a1[(i & 1) * 2], at[(i & 1) * 2]);
-            step2<NP>(make_float2(__uint_as_float(w[2]), __uint_as_float(w[3])), L2, nR2, G2,
-                      a1[(i & 1) * 2 + 1], at[(i & 1) * 2 + 1]);
+            float f[4] = {__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
+                          __uint_as_float(w[3])};
+            if constexpr (ENT) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) f[j] = max_nan_f32(f[j], kFloorF32);
+            }
+            step2<NP, ENT>(make_float2(f[0], f[1]), L2, nR2, G2, a1[(i & 1) * 2],
+                           at[(i & 1) * 2], ay[(i & 1) * 2]);
+            step2<NP, ENT>(make_float2(f[2], f[3]), L2, nR2, G2, a1[(i & 1) * 2 + 1],
+                           at[(i & 1) * 2 + 1], ay[(i & 1) * 2 + 1]);
         }
     }
     const float2 s01 = __fadd2_rn(a1[0], a1[1]), s23 = __fadd2_rn(a1[2], a1[3]);
@@ -133,6 +172,13 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
         const float2 t = __fadd2_rn(t01, t23);
         ct = t.x + t.y;
     }
+    if constexpr (ENT) {
+        const float2 y01 = __fadd2_rn(ay[0], ay[1]), y23 = __fadd2_rn(ay[2], ay[3]);
+        const float2 y = __fadd2_rn(y01, y23);
+        cy = y.x + y.y;
+    } else {
+        cy = 0.f;
+    }
 }
 
 // Rescale factor for the tau sums when the reference moves by d (log2 units).
@@ -140,6 +186,23 @@ template <int NP>
 __device__ __forceinline__ float tau_scale(float d, float g) {
     if constexpr (NP == 0) return ex2(d * g);
     else return ex2(d * (float)NP);
+}
+
+// Moves the reference of `a` from a.R to Rn >= a.R.  With y' = y - D,
+// D = Rn - R: sum 2^y' = 2^-D S1 and sum 2^y' y' = 2^-D (Y1 - D S1).
+template <int NP, bool ENT>
+__device__ __forceinline__ Acc rebase(Acc a, float Rn, float g) {
+    if (a.R == -INFINITY) {            // empty so far (or only -inf): nothing to move
+        a.R = Rn;
+        return a;
+    }
+    const float d = a.R - Rn;          // <= 0
+    const float f = ex2(d);
+    if constexpr (ENT) a.y1 = f * fmaf(d, a.s1, a.y1);
+    a.s1 *= f;
+    if constexpr (NP != 1) a.st *= tau_scale<NP>(d, g);
+    a.R = Rn;
+    return a;
 }
 
 // Load one lane's VPL vectors of a stage; vectors past the chunk read as -inf.
@@ -163,9 +226,8 @@ __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
 // lane's first chunk of a row, whose reference is still -inf).  Re-reads the
 // lane's vectors from shared memory, raises R to their maximum, rescales the
 // running sums and adds the chunk.
-template <int DT, int NP, int VPL>
-__device__ __noinline__ float3 slow_chunk(const uint4 *v4, int nvec, int lane, float g, float R,
-                                          float s1, float st) {
+template <int DT, int NP, bool ENT, int VPL>
+__device__ __noinline__ Acc slow_chunk(const uint4 *v4, int nvec, int lane, float g, Acc a) {
     uint4 q[VPL];
     load_vecs<DT, VPL>(v4, nvec, lane, q);
     float m = -INFINITY;
@@ -189,49 +251,50 @@ __device__ __noinline__ float3 slow_chunk(const uint4 *v4, int nvec, int lane, f
     }
     if (nan_seen) {
         const float qn = __int_as_float(0x7fc00000);
-        return make_float3(R, qn, qn);
+        a.s1 = a.st = a.y1 = qn;
+        return a;
     }
-    const float Rm = m * kLog2e;
-    const float Rn = fmaxf(R, Rm);
-    if (Rn == -INFINITY) return make_float3(R, s1, st);   // only -inf so far: nothing to add
-    if (Rn > R) {
-        const float d = R - Rn;    // -inf when R was -inf: the old sums are 0 anyway
-        s1 *= ex2(d);
-        if constexpr (NP != 1) st *= tau_scale<NP>(d, g);
-        R = Rn;
-    }
-    float c1, ct;
-    sum_vecs<DT, NP, VPL>(q, R, g, c1, ct);
-    s1 += c1;
-    if constexpr (NP != 1) st += ct;
-    return make_float3(R, s1, st);
+    const float Rn = fmaxf(a.R, m * kLog2e);
+    if (Rn == -INFINITY) return a;     // only -inf so far: nothing to add
+    if (Rn > a.R) a = rebase<NP, ENT>(a, Rn, g);
+    float c1, ct, cy;
+    sum_vecs<DT, NP, ENT, VPL>(q, a.R, g, c1, ct, cy);
+    a.s1 += c1;
+    if constexpr (NP != 1) a.st += ct;
+    if constexpr (ENT) a.y1 += cy;
+    return a;
 }
 
-// Merge partial b into a (both relative to their own reference).
-template <int NP>
-__device__ __forceinline__ void merge_part(float &R, float &s1, float &st, float Rb, float s1b,
-                                           float stb, float g) {
-    const float M = fmaxf(R, Rb);
-    if (M == -INFINITY) {          // both parts saw only -inf logits
-        s1 += s1b;                 // keeps a NaN poison, else 0
-        st += stb;
-        return;
+// Merge part b into a (each relative to its own reference).
+template <int NP, bool ENT>
+__device__ __forceinline__ Acc merge_part(Acc a, Acc b, float g) {
+    const float M = fmaxf(a.R, b.R);
+    if (M == -INFINITY) {              // both parts saw only -inf logits
+        a.s1 += b.s1;                  // keeps a NaN poison, else 0
+        a.st += b.st;
+        a.y1 += b.y1;
+        return a;
     }
-    const float da = R - M, db = Rb - M;
-    s1 = s1 * ex2(da) + s1b * ex2(db);
-    if constexpr (NP != 1) st = st * tau_scale<NP>(da, g) + stb * tau_scale<NP>(db, g);
-    R = M;
+    a = rebase<NP, ENT>(a, M, g);
+    b = rebase<NP, ENT>(b, M, g);
+    a.s1 += b.s1;
+    if constexpr (NP != 1) a.st += b.st;
+    if constexpr (ENT) a.y1 += b.y1;
+    return a;
 }
 
-template <int NP>
-__device__ __forceinline__ void warp_merge(float &R, float &s1, float &st, float g) {
+template <int NP, bool ENT>
+__device__ __forceinline__ Acc warp_merge(Acc a, float g) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const float Rb = __shfl_xor_sync(0xffffffffu, R, off);
-        const float s1b = __shfl_xor_sync(0xffffffffu, s1, off);
-        const float stb = __shfl_xor_sync(0xffffffffu, st, off);
-        merge_part<NP>(R, s1, st, Rb, s1b, stb, g);
+        Acc b;
+        b.R = __shfl_xor_sync(0xffffffffu, a.R, off);
+        b.s1 = __shfl_xor_sync(0xffffffffu, a.s1, off);
+        b.st = (NP != 1) ? __shfl_xor_sync(0xffffffffu, a.st, off) : 0.f;
+        b.y1 = ENT ? __shfl_xor_sync(0xffffffffu, a.y1, off) : 0.f;
+        a = merge_part<NP, ENT>(a, b, g);
     }
+    return a;
 }
 
 // -ln(1 + 2^a) in float64 (the value is computed in float, except for the tiny
@@ -242,36 +305,59 @@ __device__ __forceinline__ double neg_log1p_exp2(float a) {
     return -exp2((double)a);
 }
 
-template <int NP>
-__device__ void finalize_row(const RowsParams &p, int64_t r, float R, float s1, float st,
-                             float lt, bool bad) {
-    double o0, oq;
+// Entropy in nats from S1, Y1 (the sums without the token) and the token's
+// exponent t, all relative to the same reference; computed in float64 after
+// scaling by the larger of 2^t and S1.
+__device__ double entropy_nats(double s1, double y1, double t) {
+    const bool tok = t != -INFINITY;
+    // no other finite logit: the token holds all the mass (its exponent is +inf
+    // then, since the reference never left -inf)
+    if (!(s1 > 0.0)) return tok ? 0.0 : __longlong_as_double(0x7ff8000000000000ll);
+    const double m = fmax(tok ? t : -INFINITY, log2(s1));
+    if (m == -INFINITY) return __longlong_as_double(0x7ff8000000000000ll);
+    const double et = tok ? exp2(t - m) : 0.0;
+    const double zs = s1 * exp2(-m) + et;
+    const double ms = y1 * exp2(-m) + (tok ? t * et : 0.0);
+    return 0.6931471805599453 * (m + log2(zs) - ms / zs);
+}
+
+template <int NP, bool ENT>
+__device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bool bad) {
+    double o0, oq, h = 0.0;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
     if (bad || __float_as_uint(lt) == kAbsent) {
-        o0 = oq = qnan;
+        o0 = oq = h = qnan;
     } else {
-        const float t = fmaf(lt, kLog2e, -R);
-        const bool nonfinite = (lt != lt) || (lt == INFINITY) || (R != R) || (s1 != s1) ||
-                               (st != st) || (R == INFINITY) || (t != t);
+        if constexpr (NP == 1) a.st = a.s1;
+        const float t = fmaf(lt, kLog2e, -a.R);
+        const bool nonfinite = (lt != lt) || (lt == INFINITY) || (a.R != a.R) ||
+                               (a.s1 != a.s1) || (a.st != a.st) || (a.R == INFINITY) ||
+                               (t != t) || (ENT && (a.y1 != a.y1));
         if (nonfinite) {
             set_status(p.status, PS_DEV_NONFINITE);
-            o0 = oq = qnan;
+            o0 = oq = h = qnan;
         } else {
-            o0 = neg_log1p_exp2(s1 > 0.f ? log2f(s1) - t : -INFINITY);
+            o0 = neg_log1p_exp2(a.s1 > 0.f ? log2f(a.s1) - t : -INFINITY);
             if constexpr (NP == 1) {
                 oq = o0;
             } else {
                 const float gt = (NP == 0) ? t * p.g : t * (float)NP;
-                oq = neg_log1p_exp2(st > 0.f ? log2f(st) - gt : -INFINITY);
+                oq = neg_log1p_exp2(a.st > 0.f ? log2f(a.st) - gt : -INFINITY);
+            }
+            if constexpr (ENT) {
+                // a token logit of -inf has no mass: t = -inf leaves it out
+                h = entropy_nats((double)a.s1, (double)a.y1,
+                                 lt == -INFINITY ? -INFINITY : (double)t);
             }
         }
     }
     p.lp0[r] = o0;
     p.lq[r] = oq;
+    if constexpr (ENT) p.entropy[r] = h;
 }
 
 // WARPS warps per CTA, each with a ring of STAGES stages of SB bytes.
-template <int DT, int NP, int WARPS, int STAGES, int SB>
+template <int DT, int NP, bool ENT, int WARPS, int STAGES, int SB>
 __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kWarpsPerCta = WARPS;
@@ -305,7 +391,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
         fence_mbar_init();
     }
     __syncwarp();
-
     const uint64_t policy = l2_evict_first_policy();   // logits are read once
 
     // ---- issue side: next chunk to copy and a lane-parallel cache of row_index
@@ -372,7 +457,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
     };
     row_start();
 
-    float R = -INFINITY, s1 = 0.f, st = 0.f;
+    Acc acc = acc_empty();
     float ltok = __uint_as_float(kAbsent);
     uint32_t phase = 0;
     int s = 0;                                        // stage of chunk c
@@ -428,16 +513,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             const int nvec = (int)(bytes >> 4);
             uint4 q[kVecPerLane];
             load_vecs<DT, kVecPerLane>(v4, nvec, lane, q);
-            float c1, ct;
-            sum_vecs<DT, NP, kVecPerLane>(q, R, g, c1, ct);
+            float c1, ct, cy;
+            sum_vecs<DT, NP, ENT, kVecPerLane>(q, acc.R, g, c1, ct, cy);
             if (fmaxf(c1, ct) <= kLimit) {
-                s1 += c1;
-                if constexpr (NP != 1) st += ct;
+                acc.s1 += c1;
+                if constexpr (NP != 1) acc.st += ct;
+                if constexpr (ENT) acc.y1 += cy;
             } else {
-                const float3 r3 = slow_chunk<DT, NP, kVecPerLane>(v4, nvec, lane, g, R, s1, st);
-                R = r3.x;
-                s1 = r3.y;
-                st = r3.z;
+                acc = slow_chunk<DT, NP, ENT, kVecPerLane>(v4, nvec, lane, g, acc);
             }
         }
         __syncwarp();
@@ -445,12 +528,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
 
         const bool row_end = (k == cpr - 1) || (c == ce - 1);
         if (row_end) {
-            if constexpr (NP == 1) st = s1;
-            warp_merge<NP>(R, s1, st, g);
+            acc = warp_merge<NP, ENT>(acc, g);
             const float lt = __shfl_sync(0xffffffffu, ltok, 0);
             const int64_t rc0 = row * cpr, rc1 = rc0 + cpr;
             if (rc0 >= cb && rc1 <= ce) {
-                if (lane == 0) finalize_row<NP>(p, row, R, s1, st, lt, bad);
+                if (lane == 0) finalize_row<NP, ENT>(p, row, acc, lt, bad);
             } else {
                 const int64_t slot = (row == cb / cpr) ? 2 * vw : 2 * vw + 1;
                 const int64_t owner = warp_of_chunk(rc0, C, W);
@@ -458,10 +540,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
                 int last = 0;
                 if (lane == 0) {
                     RowPart part;
-                    part.R = R;
-                    part.s1 = s1;
-                    part.st = st;
+                    part.R = acc.R;
+                    part.s1 = acc.s1;
+                    part.st = acc.st;
                     part.ltok = lt;
+                    part.y1 = acc.y1;
+                    part.pad[0] = part.pad[1] = part.pad[2] = 0.f;
                     p.parts[slot] = part;
                     __threadfence();
                     const int old = atomicAdd(p.counters + owner, 1);
@@ -470,30 +554,30 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    float Rm = -INFINITY, s1m = 0.f, stm = 0.f;
+                    Acc m = acc_empty();
                     float ltm = __uint_as_float(kAbsent);
                     // lanes take the parts in warp order, then a fixed butterfly
                     for (int64_t u = owner + lane; u <= lastw; u += 32) {
-                        const int64_t su = (row == range_begin(u, C, W) / cpr) ? 2 * u : 2 * u + 1;
+                        const int64_t su =
+                            (row == range_begin(u, C, W) / cpr) ? 2 * u : 2 * u + 1;
                         const float4 pv = __ldcg(reinterpret_cast<const float4 *>(p.parts + su));
-                        merge_part<NP>(Rm, s1m, stm, pv.x, pv.y, pv.z, g);
+                        const float py = __ldcg(&p.parts[su].y1);
+                        m = merge_part<NP, ENT>(m, Acc{pv.x, pv.y, pv.z, py}, g);
                         if (__float_as_uint(pv.w) != kAbsent) ltm = pv.w;
                     }
-                    warp_merge<NP>(Rm, s1m, stm, g);
+                    m = warp_merge<NP, ENT>(m, g);
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
                         const float other = __shfl_xor_sync(0xffffffffu, ltm, o);
                         if (__float_as_uint(ltm) == kAbsent) ltm = other;
                     }
                     if (lane == 0) {
-                        finalize_row<NP>(p, row, Rm, s1m, stm, ltm, bad);
+                        finalize_row<NP, ENT>(p, row, m, ltm, bad);
                         p.counters[owner] = 0;
                     }
                 }
             }
-            R = -INFINITY;
-            s1 = 0.f;
-            st = 0.f;
+            acc = acc_empty();
             ltok = __uint_as_float(kAbsent);
         }
         if (++k == cpr) {
@@ -509,9 +593,9 @@ constexpr size_t smem_bytes_for() {
     return (size_t)WARPS * STAGES * SB + (size_t)WARPS * STAGES * 8;
 }
 
-template <int DT, int NP>
+template <int DT, int NP, bool ENT>
 cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    auto kern = score_rows_kernel<DT, NP, kWarpsPerCta, kStages, kStageBytes>;
+    auto kern = score_rows_kernel<DT, NP, ENT, kWarpsPerCta, kStages, kStageBytes>;
     const size_t smem = smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -520,14 +604,14 @@ cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, bool ENT>
 cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
     switch (p.npow) {
-        case 1: return launch_t<DT, 1>(p, n_ctas, stream);
-        case 2: return launch_t<DT, 2>(p, n_ctas, stream);
-        case 4: return launch_t<DT, 4>(p, n_ctas, stream);
-        case 8: return launch_t<DT, 8>(p, n_ctas, stream);
-        default: return launch_t<DT, 0>(p, n_ctas, stream);
+        case 1: return launch_t<DT, 1, ENT>(p, n_ctas, stream);
+        case 2: return launch_t<DT, 2, ENT>(p, n_ctas, stream);
+        case 4: return launch_t<DT, 4, ENT>(p, n_ctas, stream);
+        case 8: return launch_t<DT, 8, ENT>(p, n_ctas, stream);
+        default: return launch_t<DT, 0, ENT>(p, n_ctas, stream);
     }
 }
 
@@ -536,8 +620,12 @@ cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
 size_t score_rows_smem_bytes() { return smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>(); }
 
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    if (p.dtype == PS_BF16) return launch_dt<PS_BF16>(p, n_ctas, stream);
-    return launch_dt<PS_F32>(p, n_ctas, stream);
+    const bool ent = p.entropy != nullptr;
+    if (p.dtype == PS_BF16)
+        return ent ? launch_dt<PS_BF16, true>(p, n_ctas, stream)
+                   : launch_dt<PS_BF16, false>(p, n_ctas, stream);
+    return ent ? launch_dt<PS_F32, true>(p, n_ctas, stream)
+               : launch_dt<PS_F32, false>(p, n_ctas, stream);
 }
 
 }  // namespace ps

@@ -7,7 +7,11 @@ Tolerances (from the benchmark spec of the parity bar):
   log A: |gpu - oracle| <= 1e-3 absolute;
   walk: path, end node, k_Delta and reached state identical, except after a
       decision with |log u - log A| < 1e-3, where the GPU walk must still be
-      the walk its own log A values give.
+      the walk its own log A values give;
+  entropy of p0: |gpu - oracle| <= 1e-4 |oracle| + 2e-6 nats (float sums of
+      up to 262144 terms, finalised in float64);
+  epsilon classes: identical, except for decisions whose log A lies within
+      1e-3 of log eps or log(1 - eps) (the log A tolerance).
 """
 
 from __future__ import annotations
@@ -23,18 +27,24 @@ TOK_RTOL = 1e-4
 TOK_ATOL = 1e-300
 LA_ATOL = 1e-3
 NEAR_TIE = 1e-3
+ENT_RTOL = 1e-4
+ENT_ATOL = 2e-6
+EPS = 0.01
 
 
-def run_gpu(w, per_row: bool = True, sums: bool = True, stream=None) -> dict:
+def run_gpu(w, per_row: bool = True, sums: bool = True, stream=None,
+            entropy: bool = True) -> dict:
     d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
                                 V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
-                                row_index=w.row_index, per_row=per_row, sums=sums)
+                                row_index=w.row_index, per_row=per_row, sums=sums,
+                                entropy=entropy, eps=EPS)
     d.step(stream)
     torch.cuda.synchronize()
     out = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v)
            for k, v in d.t.items()
            if k in ("lp0", "lq", "lp_y", "lq_y", "lp_x", "lq_x", "log_ratio", "log_accept",
-                    "status", "wstatus", "state_seg", "end_node", "k_delta", "path")
+                    "status", "wstatus", "state_seg", "end_node", "k_delta", "path",
+                    "entropy", "eps_class")
            and v is not None}
     out["status"] = int(out["status"][0])
     out["wstatus"] = int(out["wstatus"][0])
@@ -42,10 +52,12 @@ def run_gpu(w, per_row: bool = True, sums: bool = True, stream=None) -> dict:
 
 
 def oracle_rows(w, block_rows: int = 8192, threads: int | None = None):
-    """Per-row oracle values, copying logits to the host block by block."""
+    """Per-row oracle values (lp0, lq, entropy), copying logits to the host
+    block by block."""
     n = w.n_rows
     lp0 = np.empty(n)
     lq = np.empty(n)
+    ent = np.empty(n)
     toks = w.tokens.cpu().numpy()
     if w.row_index is not None:
         # rows come from a pool: score each pool row used once per token
@@ -56,31 +68,33 @@ def oracle_rows(w, block_rows: int = 8192, threads: int | None = None):
         pool_tok = (uk % (w.V + 1)).astype(np.int32)
         a0 = np.empty(uk.shape[0])
         aq = np.empty(uk.shape[0])
+        ae = np.empty(uk.shape[0])
         for i0 in range(0, uk.shape[0], block_rows):
             i1 = min(uk.shape[0], i0 + block_rows)
             idx = torch.from_numpy(pool_rows[i0:i1]).to(w.logits.device)
             host = w.logits.index_select(0, idx)
             lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
             dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
-            a0[i0:i1], aq[i0:i1] = oracle.row_logprobs(lg, dt, w.V, pool_tok[i0:i1], w.tau,
-                                                       threads=threads)
-        return a0[inv], aq[inv]
+            a0[i0:i1], aq[i0:i1], ae[i0:i1] = oracle.row_logprobs(
+                lg, dt, w.V, pool_tok[i0:i1], w.tau, threads=threads, entropy=True)
+        return a0[inv], aq[inv], ae[inv]
     for r0 in range(0, n, block_rows):
         r1 = min(n, r0 + block_rows)
         host = w.logits[r0:r1]
         lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
         dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
-        lp0[r0:r1], lq[r0:r1] = oracle.row_logprobs(lg, dt, w.V, toks[r0:r1], w.tau,
-                                                    threads=threads)
-    return lp0, lq
+        lp0[r0:r1], lq[r0:r1], ent[r0:r1] = oracle.row_logprobs(
+            lg, dt, w.V, toks[r0:r1], w.tau, threads=threads, entropy=True)
+    return lp0, lq, ent
 
 
 def run_oracle(w, threads: int | None = None) -> dict:
-    lp0, lq = oracle_rows(w, threads=threads)
+    lp0, lq, ent = oracle_rows(w, threads=threads)
     sums = oracle.suffix_sums(w.layout, lp0, lq)
     r, la = oracle.log_accept(sums, w.alpha)
     wk = oracle.walk(w.layout, la, w.u, w.max_steps)
-    out = dict(lp0=lp0, lq=lq, log_ratio=r, log_accept=la, walk=wk)
+    out = dict(lp0=lp0, lq=lq, entropy=ent, log_ratio=r, log_accept=la, walk=wk,
+               eps_class=oracle.eps_class(la, EPS))
     out.update(sums)
     return out
 
@@ -91,7 +105,9 @@ def check_rows(g: dict, o: dict, rtol: float = TOK_RTOL) -> dict:
         a, b = g[k], o[k]
         assert a.shape == b.shape
         assert np.array_equal(np.isnan(a), np.isnan(b)), f"{k}: NaN pattern differs"
-        m = ~np.isnan(b)
+        inf = np.isinf(b)          # a masked token: -inf on both sides
+        assert np.array_equal(a[inf], b[inf]), f"{k}: infinite values differ"
+        m = ~np.isnan(b) & ~inf
         err = np.abs(a[m] - b[m])
         bound = rtol * np.abs(b[m]) + TOK_ATOL
         bad = np.nonzero(err > bound)[0]
@@ -99,6 +115,14 @@ def check_rows(g: dict, o: dict, rtol: float = TOK_RTOL) -> dict:
                                f"{np.max(err / (np.abs(b[m]) + 1e-300)):.3e}")
         rel = err / np.maximum(np.abs(b[m]), 1e-300)
         stats[f"{k}_max_rel"] = float(rel.max()) if rel.size else 0.0
+    if g.get("entropy") is not None:
+        a, b = g["entropy"], o["entropy"]
+        assert np.array_equal(np.isnan(a), np.isnan(b)), "entropy: NaN pattern differs"
+        m = ~np.isnan(b)
+        err = np.abs(a[m] - b[m])
+        bad = np.nonzero(err > ENT_RTOL * np.abs(b[m]) + ENT_ATOL)[0]
+        assert bad.size == 0, f"entropy: {bad.size} rows off; worst |diff| {err.max():.3e}"
+        stats["entropy_max_abs"] = float(err.max()) if err.size else 0.0
     return stats
 
 
@@ -117,6 +141,14 @@ def check_log_accept(w, g: dict, o: dict, atol: float = LA_ATOL) -> dict:
             a, b = g[k][req], o[k][req]
             err = np.abs(a - b)
             stats[f"{k}_max_abs"] = float(np.nanmax(err)) if err.size else 0.0
+    if g.get("eps_class") is not None:
+        gc, oc = g["eps_class"], o["eps_class"]
+        assert np.all(gc[~req] == -1)
+        la = o["log_accept"]
+        near = ((np.abs(la - np.log(EPS)) < LA_ATOL) | (np.abs(la - np.log1p(-EPS)) < LA_ATOL))
+        diff = (gc != oc) & req
+        assert not np.any(diff & ~near), "epsilon classes differ away from the thresholds"
+        stats["eps_class_near_threshold"] = int(np.sum(diff))
     return stats
 
 

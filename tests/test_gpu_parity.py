@@ -133,6 +133,27 @@ def test_dominant_token_keeps_relative_accuracy():
         assert (o["lq"] < 0).all() and (o["lq"] > -1e-40).all()
 
 
+def test_entropy_edge_cases():
+    # uniform rows (H = log V), one-token rows (H = 0), a peaked row, masked
+    # entries and a masked token: entropy and log-probabilities against the oracle
+    V = 151936
+    w = _small(V, "bf16", T=8, n_pf=3, n_chains=1, seed=21)
+    x = w.logits.clone()
+    x[0] = 0.5                                   # uniform
+    x[1] = float("-inf")
+    x[1, 5] = 2.0                                # a single finite logit
+    w.tokens[1] = 5
+    x[2] = 0.0
+    x[2, 9] = 30.0                               # peaked
+    x[3, 2000:] = float("-inf")                  # masked tail
+    w.logits = x
+    g = H.run_gpu(w)
+    o = H.run_oracle(w)
+    s = H.check_rows(g, o)
+    _report("entropy edges", s)
+    assert abs(g["entropy"][0] - np.log(V)) < 1e-4 and g["entropy"][1] == 0.0
+
+
 def test_masked_vocabulary():
     w = _small(151936, "bf16", T=10, n_pf=4, n_chains=2, seed=11)
     x = w.logits.clone()
