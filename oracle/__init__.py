@@ -14,7 +14,11 @@ Sampling" (arXiv 2610.13171) in float64, step by step and without shortcuts:
                         child keeps its parent's state; Condition 1);
 * ``suffix_sums``       log p0 / log q_tau of the y and x suffixes by summing
                         token log-probabilities over positions c+1..T
-                        (eq. (6), Appendix B.1 eq. (7)-(9));
+                        (eq. (6), Appendix B.1 eq. (7)-(9)), optionally with the
+                        current state's values carried from the previous round;
+* ``carry_state``       the reached state's per-position values for the next
+                        round, with eq. (21) log-likelihood and eq. (22)
+                        confidence (section 3.2 step (3));
 * ``log_accept``        log A = min{0, log q(x|y) - log q(y|x) + alpha (log p0(y) - log p0(x))}
                         (eq. (6));
 * ``walk``              the MH walk over the subtree: accept iff u <= A, left
@@ -200,12 +204,31 @@ def materialize(layout, c: int) -> ChainStates:
     return ChainStates(T=T, root_seg=root, rows=rows, state_seg=state_seg)
 
 
-def suffix_sums(layout, lp0: np.ndarray, lq: np.ndarray, states=None) -> dict:
+def _pos_values(st_rows, c, row_vals, root_vals, T, t0=1):
+    """Values of positions t0..T of one state (index t of the returned array is
+    position t): the row value where the state has a scored row, else the
+    chain root's carried value for that position."""
+    out = np.full(T + 1, np.nan)
+    rows = np.asarray(st_rows[t0:T + 1], dtype=np.int64)
+    has = rows >= 0
+    vals = np.asarray(row_vals)[np.where(has, rows, 0)]
+    if not has.all():
+        assert root_vals is not None, "root position without a row or a carried value"
+        vals = np.where(has, vals, np.asarray(root_vals)[c, t0 - 1:T])
+    out[t0:] = vals
+    return out
+
+
+def suffix_sums(layout, lp0: np.ndarray, lq: np.ndarray, states=None,
+                root_lp0: np.ndarray | None = None, root_lq: np.ndarray | None = None) -> dict:
     """LP_y, LQ_y, LP_x, LQ_x for every request (NaN at chain roots).
 
     For the request s issued at node v with cut c_s: the y suffix is positions
     c_s+1..T of the acceptance child's state, the x suffix the same positions of
     state(v); each sum adds token log-probabilities (eq. (6) and the sum under it).
+    Positions of the current state that have no scored row take the values the
+    previous round retained (root_lp0/root_lq [n_chains, T], position t at
+    column t-1; section 3.2 step (3)).
     """
     n = layout.n_seg
     out = {k: np.full(n, np.nan) for k in ("lp_y", "lq_y", "lp_x", "lq_x")}
@@ -219,13 +242,42 @@ def suffix_sums(layout, lp0: np.ndarray, lq: np.ndarray, states=None) -> dict:
                 continue
             cs = int(layout.seg_cut[s])
             a = int(layout.acc[n0 + v]) - n0
-            yrows = st.rows[a][cs + 1:T + 1]
-            xrows = st.rows[v][cs + 1:T + 1]
-            assert (yrows >= 0).all() and (xrows >= 0).all()
-            out["lp_y"][s] = np.sum(lp0[yrows])
-            out["lq_y"][s] = np.sum(lq[yrows])
-            out["lp_x"][s] = np.sum(lp0[xrows])
-            out["lq_x"][s] = np.sum(lq[xrows])
+            vy0 = _pos_values(st.rows[a], c, lp0, root_lp0, T, cs + 1)
+            vyq = _pos_values(st.rows[a], c, lq, root_lq, T, cs + 1)
+            vx0 = _pos_values(st.rows[v], c, lp0, root_lp0, T, cs + 1)
+            vxq = _pos_values(st.rows[v], c, lq, root_lq, T, cs + 1)
+            out["lp_y"][s] = np.sum(vy0[cs + 1:])
+            out["lq_y"][s] = np.sum(vyq[cs + 1:])
+            out["lp_x"][s] = np.sum(vx0[cs + 1:])
+            out["lq_x"][s] = np.sum(vxq[cs + 1:])
+    return out
+
+
+def carry_state(layout, state_seg: np.ndarray, row_vals: dict, prev: dict) -> dict:
+    """The reached state's retained per-position values for the next round
+    (section 3.2 step (3): the sampler keeps the token-level log-probabilities
+    of the state it moves to), and the statistics of eq. (21) and (22).
+
+    row_vals: per-row arrays of this batch, e.g. {"lp0": .., "lq": .., "entropy": ..};
+    prev: the same keys, each [n_chains, T]: the values of the current state,
+    used for positions below the root cut.  Returns [n_chains, T] arrays with
+    the same keys, plus "loglik" = mean of lp0 over positions 1..T (eq. (21))
+    and, when entropy is given, "confidence" = minus the mean entropy (eq. (22)).
+    """
+    T = layout.T
+    nc = layout.n_chains
+    out = {k: np.empty((nc, T)) for k in row_vals}
+    for c in range(nc):
+        st = materialize(layout, c)
+        s = int(state_seg[c])
+        # a node holding the reached state: any node whose state came from s
+        v = next(i for i, x in enumerate(st.state_seg) if x == s and st.rows[i] is not None)
+        for k, vals in row_vals.items():
+            pv = _pos_values(st.rows[v], c, vals, prev.get(k), T)
+            out[k][c] = pv[1:]
+    out["loglik"] = out["lp0"].mean(axis=1)
+    if "entropy" in out:
+        out["confidence"] = -out["entropy"].mean(axis=1)
     return out
 
 
