@@ -101,6 +101,13 @@ typedef enum { PS_BF16 = 0, PS_F32 = 1 } ps_dtype;
  * alpha, tau   power exponent (finite) and proposal temperature (> 0).
  * eps          epsilon of the epsilon-certainty classes (section 3.3), in
  *              (0, 1/2); read only when ps_score_out.eps_class is requested.
+ * root_lp0, root_lq  optional [n_chains][T] float64 (position t at t-1): the
+ *              current state's token log-probabilities retained from the
+ *              previous round (ps_carry_state).  When given, positions up to a
+ *              chain root's cut take these values instead of rows, and a
+ *              request's cut may lie below the root's cut; a root cut of T
+ *              means the current state needs no scored rows at all.  When NULL,
+ *              every request's cut must be >= its root's cut.
  */
 typedef struct {
     int32_t V;
@@ -122,6 +129,8 @@ typedef struct {
     const void *logits;
     const int64_t *row_index;
     const int32_t *tokens;
+    const double *root_lp0;
+    const double *root_lq;
 } ps_subtree_batch;
 
 /*
@@ -199,6 +208,48 @@ ps_status ps_score_rows(const ps_subtree_batch *batch, double *lp0, double *lq, 
                         void *cuda_stream);
 ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
                               const double *lq, const ps_score_out *out, void *cuda_stream);
+
+/*
+ * Round carry-over (section 3.2 step (3): after the walk the sampler keeps the
+ * reached state's token-level log-probabilities for the next round's
+ * acceptance computations).  For every chain, the reached state
+ * x_Delta = x_{0:c*} + y^{s*} (s* = state_seg, c* its cut; x itself when s* is
+ * the root) gives per-position values for positions 1..T: the previous
+ * round's values up to the root's cut, root rows up to c*, then the rows of
+ * s*.  Optionally also eq. (21) (length-normalised log-likelihood, the mean of
+ * lp0 over positions 1..T) and eq. (22) (confidence, minus the mean entropy).
+ *
+ * state_seg        [n_chains] int32, from ps_walk_subtree.
+ * row_lp0, row_lq  [n_rows] per-row values of this batch (ps_score_rows);
+ * row_entropy      [n_rows] optional.
+ * prev_lp0, prev_lq, prev_entropy   [n_chains][T] the current state's values;
+ *                  read only at positions up to a root's cut (may be NULL when
+ *                  every root cut is 0, or equal to the batch's root_lp0/lq).
+ * next_lp0, next_lq  [n_chains][T] out, required; next_entropy optional (needs
+ *                  row_entropy, and prev_entropy when a root cut is > 0).
+ * loglik, confidence  [n_chains] optional (confidence needs next_entropy).
+ * status           device int32 word, required (PS_DEV_BAD_LAYOUT when a needed
+ *                  input is missing or state_seg is not a segment of its chain;
+ *                  that chain's outputs are NaN).
+ */
+typedef struct {
+    const int32_t *state_seg;
+    const double *row_lp0;
+    const double *row_lq;
+    const double *row_entropy;
+    const double *prev_lp0;
+    const double *prev_lq;
+    const double *prev_entropy;
+    double *next_lp0;
+    double *next_lq;
+    double *next_entropy;
+    double *loglik;
+    double *confidence;
+    int32_t *status;
+} ps_carry_io;
+
+ps_status ps_carry_state(const ps_subtree_batch *batch, const ps_carry_io *io,
+                         void *cuda_stream);
 
 /*
  * ps_score_subtree_noalloc: the same scoring as ps_score_subtree, for callers

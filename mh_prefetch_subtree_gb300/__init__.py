@@ -8,8 +8,8 @@ raises.
 
 Entry points (see include/ps.h for the contract):
     ps_score_workspace_bytes, ps_score_subtree, ps_score_rows,
-    ps_assemble_subtree, ps_walk_subtree, ps_validate_subtree,
-    ps_status_string, ps_version
+    ps_assemble_subtree, ps_walk_subtree, ps_carry_state, ps_validate_subtree,
+    ps_score_subtree_noalloc, ps_status_string, ps_version
 Convenience: ``make_batch``, ``make_score_out``, ``make_tree``,
 ``make_walk_out`` build the structs from tensors; ``DeviceSubtree`` holds a
 whole batch on the GPU with its outputs and workspace.
@@ -45,7 +45,8 @@ class PsSubtreeBatch(ctypes.Structure):
                 ("ld", ctypes.c_int64), ("n_logit_rows", ctypes.c_int64),
                 ("alpha", ctypes.c_double), ("tau", ctypes.c_double),
                 ("eps", ctypes.c_double), ("chain_seg0", _vp), ("seg_row0", _vp), ("seg_cut", _vp), ("seg_src", _vp),
-                ("logits", _vp), ("row_index", _vp), ("tokens", _vp)]
+                ("logits", _vp), ("row_index", _vp), ("tokens", _vp),
+                ("root_lp0", _vp), ("root_lq", _vp)]
 
 
 class PsScoreOut(ctypes.Structure):
@@ -63,6 +64,12 @@ class PsTree(ctypes.Structure):
 
 class PsWalkOut(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("state_seg", "end_node", "k_delta", "path", "status")]
+
+
+class PsCarryIo(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("state_seg", "row_lp0", "row_lq", "row_entropy", "prev_lp0",
+                                   "prev_lq", "prev_entropy", "next_lp0", "next_lq",
+                                   "next_entropy", "loglik", "confidence", "status")]
 
 
 class PsError(RuntimeError):
@@ -98,6 +105,9 @@ def lib() -> ctypes.CDLL:
         L.ps_score_subtree_noalloc.restype = ctypes.c_int
         L.ps_walk_subtree.argtypes = [ctypes.POINTER(PsTree), _vp, ctypes.POINTER(PsWalkOut), _vp]
         L.ps_walk_subtree.restype = ctypes.c_int
+        L.ps_carry_state.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsCarryIo),
+                                     _vp]
+        L.ps_carry_state.restype = ctypes.c_int
         L.ps_validate_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsTree),
                                           ctypes.c_char_p, ctypes.c_size_t]
         L.ps_validate_subtree.restype = ctypes.c_int
@@ -183,6 +193,35 @@ def ps_walk_subtree(tree: PsTree, log_accept: torch.Tensor, out: PsWalkOut, stre
     return st
 
 
+def ps_carry_state(batch: PsSubtreeBatch, io: PsCarryIo, stream=None, check: bool = True) -> int:
+    """The reached state's per-position values for the next round (see
+    include/ps.h)."""
+    st = lib().ps_carry_state(ctypes.byref(batch), ctypes.byref(io), _stream(stream, None))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_carry_state")
+    return st
+
+
+def make_carry_io(*, state_seg, row_lp0, row_lq, next_lp0, next_lq, status, row_entropy=None,
+                  prev_lp0=None, prev_lq=None, prev_entropy=None, next_entropy=None,
+                  loglik=None, confidence=None) -> PsCarryIo:
+    io = PsCarryIo()
+    _need(state_seg, torch.int32, "state_seg")
+    _need(status, torch.int32, "status")
+    io.state_seg, io.status = _ptr(state_seg), _ptr(status)
+    for name, x, opt in (("row_lp0", row_lp0, False), ("row_lq", row_lq, False),
+                         ("row_entropy", row_entropy, True), ("prev_lp0", prev_lp0, True),
+                         ("prev_lq", prev_lq, True), ("prev_entropy", prev_entropy, True),
+                         ("next_lp0", next_lp0, False), ("next_lq", next_lq, False),
+                         ("next_entropy", next_entropy, True), ("loglik", loglik, True),
+                         ("confidence", confidence, True)):
+        _need(x, torch.float64, name, optional=opt)
+        setattr(io, name, _ptr(x))
+    io._keep = (state_seg, row_lp0, row_lq, row_entropy, prev_lp0, prev_lq, prev_entropy,
+                next_lp0, next_lq, next_entropy, loglik, confidence, status)
+    return io
+
+
 def ps_validate_subtree(batch: PsSubtreeBatch | None, tree: PsTree | None) -> tuple[int, str]:
     buf = ctypes.create_string_buffer(256)
     st = lib().ps_validate_subtree(ctypes.byref(batch) if batch is not None else None,
@@ -239,7 +278,8 @@ def _need(x, dtype: torch.dtype, name: str, optional: bool = False):
 def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0, seg_cut,
                seg_src, logits=None, tokens=None, row_index=None, n_rows: int | None = None,
                n_logit_rows: int | None = None, ld: int | None = None,
-               dtype: int | None = None, eps: float = 0.01) -> PsSubtreeBatch:
+               dtype: int | None = None, eps: float = 0.01, root_lp0=None,
+               root_lq=None) -> PsSubtreeBatch:
     """Fill a ps_subtree_batch from tensors (device for scoring, host for validation)."""
     _need(chain_seg0, torch.int32, "chain_seg0")
     _need(seg_row0, torch.int64, "seg_row0")
@@ -247,6 +287,8 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
     _need(seg_src, torch.int32, "seg_src")
     _need(tokens, torch.int32, "tokens", optional=True)
     _need(row_index, torch.int64, "row_index", optional=True)
+    _need(root_lp0, torch.float64, "root_lp0", optional=True)
+    _need(root_lq, torch.float64, "root_lq", optional=True)
     b = PsSubtreeBatch()
     b.V, b.T = int(V), int(T)
     b.n_chains = int(chain_seg0.shape[0]) - 1
@@ -277,7 +319,9 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
     b.chain_seg0, b.seg_row0 = _ptr(chain_seg0), _ptr(seg_row0)
     b.seg_cut, b.seg_src = _ptr(seg_cut), _ptr(seg_src)
     b.logits, b.row_index, b.tokens = _ptr(logits), _ptr(row_index), _ptr(tokens)
-    b._keep = (chain_seg0, seg_row0, seg_cut, seg_src, logits, tokens, row_index)
+    b.root_lp0, b.root_lq = _ptr(root_lp0), _ptr(root_lq)
+    b._keep = (chain_seg0, seg_row0, seg_cut, seg_src, logits, tokens, row_index, root_lp0,
+               root_lq)
     return b
 
 
@@ -350,7 +394,9 @@ class DeviceSubtree:
     def create(cls, *, layout, u, logits: torch.Tensor, tokens: torch.Tensor, V: int,
                alpha: float, tau: float, max_steps: int, row_index: torch.Tensor | None = None,
                per_row: bool = True, sums: bool = True, path: bool = True,
-               entropy: bool = False, eps: float | None = None) -> "DeviceSubtree":
+               entropy: bool = False, eps: float | None = None,
+               root_lp0: torch.Tensor | None = None,
+               root_lq: torch.Tensor | None = None) -> "DeviceSubtree":
         dev = logits.device
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
         t = dict(
@@ -383,7 +429,8 @@ class DeviceSubtree:
         batch = make_batch(V=V, T=layout.T, alpha=alpha, tau=tau, chain_seg0=t["chain_seg0"],
                            seg_row0=t["seg_row0"], seg_cut=t["seg_cut"], seg_src=t["seg_src"],
                            logits=logits, tokens=tokens, row_index=row_index, n_rows=n_rows,
-                           eps=0.01 if eps is None else eps)
+                           eps=0.01 if eps is None else eps, root_lp0=root_lp0,
+                           root_lq=root_lq)
         ws_bytes = ps_score_workspace_bytes(batch)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         sout = make_score_out(log_accept=t["log_accept"], status=t["status"], lp0=t["lp0"],
@@ -415,3 +462,32 @@ class DeviceSubtree:
         """One pass of the whole path: score, then walk."""
         self.score(stream)
         self.walk(stream)
+
+    def carry(self, prev: dict | None = None, stream=None) -> dict:
+        """Per-position values of each chain's reached state for the next
+        round (after step()); prev holds the current state's values for the
+        positions below the root cut ("lp0", "lq" and optionally "entropy",
+        each [n_chains, T])."""
+        t = self.t
+        n_chains = int(t["chain_seg0"].shape[0]) - 1
+        T = int(self.batch.T)
+        dev = t["log_accept"].device
+        out = {k: torch.empty((n_chains, T), dtype=torch.float64, device=dev)
+               for k in ("lp0", "lq")}
+        ent = t.get("entropy") is not None
+        if ent:
+            out["entropy"] = torch.empty((n_chains, T), dtype=torch.float64, device=dev)
+        out["loglik"] = torch.empty(n_chains, dtype=torch.float64, device=dev)
+        if ent:
+            out["confidence"] = torch.empty(n_chains, dtype=torch.float64, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        prev = prev or {}
+        io = make_carry_io(state_seg=t["state_seg"], row_lp0=t["lp0"], row_lq=t["lq"],
+                           row_entropy=t.get("entropy"), prev_lp0=prev.get("lp0"),
+                           prev_lq=prev.get("lq"), prev_entropy=prev.get("entropy"),
+                           next_lp0=out["lp0"], next_lq=out["lq"],
+                           next_entropy=out.get("entropy"), loglik=out["loglik"],
+                           confidence=out.get("confidence"), status=status)
+        ps_carry_state(self.batch, io, stream)
+        out["status"] = status
+        return out

@@ -181,6 +181,7 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
     if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
     if (b->n_rows > 0 && (!lp0 || !lq)) return PS_ERR_INVALID_ARG;
+    if ((b->root_lp0 == nullptr) != (b->root_lq == nullptr)) return PS_ERR_INVALID_ARG;
     if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
     int sms = 0;
     ps_status st = device_of(out->log_accept, &sms);
@@ -197,6 +198,8 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     a.seg_src = b->seg_src;
     a.lp0 = lp0;
     a.lq = lq;
+    a.root_lp0 = b->root_lp0;
+    a.root_lq = b->root_lq;
     a.lp_y = out->lp_y;
     a.lq_y = out->lq_y;
     a.lp_x = out->lp_x;
@@ -297,7 +300,7 @@ ps_status ps_validate_subtree(const ps_subtree_batch *b, const ps_tree *t, char 
                 const int32_t csrc = src == s0 ? T : b->seg_cut[src];
                 if (cs > csrc)
                     return fail(PS_ERR_INFEASIBLE, "request %lld: c_i > c_src (%lld)", s, csrc);
-                if (cs < rc)
+                if (cs < rc && b->root_lp0 == nullptr)
                     return fail(PS_ERR_INFEASIBLE, "request %lld cut below root rows (%lld)", s,
                                 rc);
             }
@@ -479,4 +482,29 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
         if (st != PS_OK) return st;
     }
     return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
+}
+
+extern "C" ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
+                                    void *cuda_stream) {
+    if (!b || !io || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)
+        return PS_ERR_INVALID_ARG;
+    if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
+    if (!io->state_seg || !io->next_lp0 || !io->next_lq || !io->status) return PS_ERR_INVALID_ARG;
+    if (b->n_rows > 0 && (!io->row_lp0 || !io->row_lq)) return PS_ERR_INVALID_ARG;
+    if (io->next_entropy && b->n_rows > 0 && !io->row_entropy) return PS_ERR_INVALID_ARG;
+    if (io->confidence && !io->next_entropy) return PS_ERR_INVALID_ARG;
+    int sms = 0;
+    ps_status st = device_of(io->next_lp0, &sms);
+    if (st != PS_OK) return st;
+    ps::CarryParams p;
+    p.T = b->T;
+    p.n_chains = b->n_chains;
+    p.n_seg = b->n_seg;
+    p.n_rows = b->n_rows;
+    p.chain_seg0 = b->chain_seg0;
+    p.seg_row0 = b->seg_row0;
+    p.seg_cut = b->seg_cut;
+    p.seg_src = b->seg_src;
+    p.io = *io;
+    return map_cuda(ps::launch_carry(p, (cudaStream_t)cuda_stream));
 }

@@ -126,15 +126,24 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
             q1 - q0 != (int64_t)(T - csrc))
             bits |= PS_DEV_BAD_LAYOUT;
     }
-    if (bits == 0 && (cs > csrc || cs < rc)) bits |= PS_DEV_INFEASIBLE;
+    // Condition 1; and without carried root values, the root rows must cover
+    // every position a request's x suffix reads
+    if (bits == 0 && (cs > csrc || (cs < rc && p.root_lp0 == nullptr))) bits |= PS_DEV_INFEASIBLE;
 
     double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
     pdl_wait_prerequisites();                        // per-row values are now visible
     if (bits == 0) {                                 // uniform across the block
         double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
         range_sum(p.lp0, p.lq, y0 + tid, y1, a, b);
-        const int64_t x0 = r0 + (cs - rc), x1 = r0 + (csrc - rc);
-        range_sum(p.lp0, p.lq, x0 + tid, x1, e, f);
+        // the x suffix: positions cs+1..csrc of the current state (carried values
+        // up to the root's cut, root rows above it), then all rows of src
+        const int32_t k1 = min(rc, csrc);               // last carried position
+        if (cs < k1) {
+            const int64_t base = (int64_t)c * T;
+            range_sum(p.root_lp0, p.root_lq, base + cs + tid, base + k1, e, f);
+        }
+        const int32_t lo = max(cs, rc);                 // rows cover positions > rc
+        if (lo < csrc) range_sum(p.lp0, p.lq, r0 + (lo - rc) + tid, r0 + (csrc - rc), e, f);
         range_sum(p.lp0, p.lq, q0 + tid, q1, e, f);
         a = warp_sum(a);
         b = warp_sum(b);

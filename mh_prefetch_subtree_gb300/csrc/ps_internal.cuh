@@ -67,9 +67,23 @@ struct AssembleParams {
     const int32_t *seg_src;
     const double *lp0;
     const double *lq;
+    const double *root_lp0;     // optional carried values of the roots [n_chains][T]
+    const double *root_lq;
     double *lp_y, *lq_y, *lp_x, *lq_x, *log_ratio, *log_accept;
     int8_t *eps_class;
     int32_t *status;
+};
+
+struct CarryParams {
+    int32_t T;
+    int32_t n_chains;
+    int32_t n_seg;
+    int64_t n_rows;
+    const int32_t *chain_seg0;
+    const int64_t *seg_row0;
+    const int32_t *seg_cut;
+    const int32_t *seg_src;
+    ps_carry_io io;
 };
 
 struct WalkParams {
@@ -93,6 +107,7 @@ struct WalkParams {
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream);
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);
+cudaError_t launch_carry(const CarryParams &p, cudaStream_t stream);
 size_t score_rows_smem_bytes();
 
 // ---------------------------------------------------------------------------

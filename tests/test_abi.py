@@ -40,8 +40,9 @@ def test_every_declared_function_is_exported():
 
 
 def test_struct_sizes_match_the_header_layout():
-    # int32 x6, int64 x3, double x3, 7 pointers
-    assert ctypes.sizeof(ps.PsSubtreeBatch) == 6 * 4 + 3 * 8 + 3 * 8 + 7 * 8
+    # int32 x6, int64 x3, double x3, 9 pointers
+    assert ctypes.sizeof(ps.PsSubtreeBatch) == 6 * 4 + 3 * 8 + 3 * 8 + 9 * 8
+    assert ctypes.sizeof(ps.PsCarryIo) == 13 * 8
     assert ctypes.sizeof(ps.PsScoreOut) == 11 * 8
     assert ctypes.sizeof(ps.PsTree) == 4 * 4 + 6 * 8
     assert ctypes.sizeof(ps.PsWalkOut) == 5 * 8
