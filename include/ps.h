@@ -349,6 +349,50 @@ ps_status ps_walk_subtree(const ps_tree *tree, const double *log_accept,
 ps_status ps_validate_subtree(const ps_subtree_batch *batch, const ps_tree *tree,
                               char *msg, size_t msg_len);
 
+/*
+ * Host-side tree construction (synchronous; all pointers are host memory).
+ *
+ * ps_build_bfs_tree: BFS request collection for one chain (section 3.2 step
+ * (1), Example 2).  From the root (cut T) nodes are expanded in breadth-first
+ * order; expansion k uses cuts[k] (the random cut of that decision, drawn by
+ * the caller: Proposition 1, (A2)).  The acceptance child gets the cut, the
+ * rejection child keeps its parent's cut and state; a request is feasible when
+ * its cut is <= the node's cut (Condition 1), else it is deferred (req =
+ * PS_NODE_DEFERRED, deferred_cut = its cut) and its acceptance child is not
+ * expanded; the rejection child is enqueued either way.  Stops at n_pf
+ * feasible requests, an empty queue, or when the cuts run out.  depth_cap < 0
+ * means no cap (else nodes at depth >= depth_cap are not expanded: the K - k
+ * cap of Appendix C.1).
+ * Outputs (capacities max_nodes >= 1 + 2 n_cuts, max_seg >= n_pf + 1): acc,
+ * rej, req, node_cut, deferred_cut per node; seg_cut, seg_src per segment
+ * (segment 0 is the root: its cut is the smallest request cut, or T);
+ * n_nodes, n_seg, and the number of cuts used.  Returns PS_ERR_INVALID_ARG for
+ * a cut outside [0, T-1] or too small a capacity.
+ */
+ps_status ps_build_bfs_tree(int32_t T, int32_t n_pf, int32_t depth_cap, const int32_t *cuts,
+                            int32_t n_cuts, int32_t max_nodes, int32_t max_seg, int32_t *acc,
+                            int32_t *rej, int32_t *req, int32_t *node_cut,
+                            int32_t *deferred_cut, int32_t *seg_cut, int32_t *seg_src,
+                            int32_t *n_nodes, int32_t *n_seg, int32_t *n_cuts_used);
+
+/*
+ * ps_predictive_allocation: the selection of at most `budget` candidate nodes,
+ * ancestor-closed, that maximises the predicted number of completed
+ * transitions (eq. (17)), by the dynamic program of eq. (19) (Proposition 2).
+ * The caller gives a finite tree rooted at node 0 (acc, rej: child ids or -1),
+ * which nodes are candidates (expandable with all strict ancestors expandable,
+ * Appendix C.1) and each node's predicted acceptance-branch probability h_acc
+ * in [0, 1] (e.g. from class probabilities by eq. (14)).  Outputs V(v0,
+ * budget) and selected[v] = 1 for the chosen nodes (smallest m on ties).
+ * Host memory O(n_nodes * budget).  PS_ERR_BAD_TREE for an inconsistent tree.
+ */
+ps_status ps_predictive_allocation(int32_t n_nodes, const int32_t *acc, const int32_t *rej,
+                                   const uint8_t *candidate, const double *h_acc,
+                                   int32_t budget, double *value, uint8_t *selected);
+
+/* eq. (14): h(v+) = (1 + P(certain accept) - P(certain reject)) / 2 (Lemma 3). */
+double ps_midpoint_branch_probability(double p_accept, double p_reject);
+
 /* Static text for a status code. */
 const char *ps_status_string(ps_status status);
 

@@ -108,6 +108,17 @@ def lib() -> ctypes.CDLL:
         L.ps_carry_state.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsCarryIo),
                                      _vp]
         L.ps_carry_state.restype = ctypes.c_int
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        L.ps_build_bfs_tree.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32] + \
+            [_vp] * 7 + [i32p, i32p, i32p]
+        L.ps_build_bfs_tree.restype = ctypes.c_int
+        L.ps_predictive_allocation.argtypes = [ctypes.c_int32, _vp, _vp, _vp, _vp,
+                                               ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
+                                               _vp]
+        L.ps_predictive_allocation.restype = ctypes.c_int
+        L.ps_midpoint_branch_probability.argtypes = [ctypes.c_double, ctypes.c_double]
+        L.ps_midpoint_branch_probability.restype = ctypes.c_double
         L.ps_validate_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsTree),
                                           ctypes.c_char_p, ctypes.c_size_t]
         L.ps_validate_subtree.restype = ctypes.c_int
@@ -220,6 +231,51 @@ def make_carry_io(*, state_seg, row_lp0, row_lq, next_lp0, next_lq, status, row_
     io._keep = (state_seg, row_lp0, row_lq, row_entropy, prev_lp0, prev_lq, prev_entropy,
                 next_lp0, next_lq, next_entropy, loglik, confidence, status)
     return io
+
+
+def ps_build_bfs_tree(T: int, n_pf: int, depth_cap: int | None, cuts) -> dict:
+    """BFS request collection for one chain (host; see include/ps.h)."""
+    cuts = np.ascontiguousarray(cuts, dtype=np.int32)
+    n_cuts = int(cuts.shape[0])
+    max_nodes, max_seg = 1 + 2 * n_cuts, n_pf + 1
+    arr = {k: np.empty(max_nodes, np.int32) for k in ("acc", "rej", "req", "node_cut",
+                                                      "deferred_cut")}
+    seg = {k: np.empty(max_seg, np.int32) for k in ("seg_cut", "seg_src")}
+    nn, ns, used = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().ps_build_bfs_tree(int(T), int(n_pf), -1 if depth_cap is None else int(depth_cap),
+                                 cuts.ctypes.data if n_cuts else None, n_cuts, max_nodes,
+                                 max_seg, arr["acc"].ctypes.data, arr["rej"].ctypes.data,
+                                 arr["req"].ctypes.data, arr["node_cut"].ctypes.data,
+                                 arr["deferred_cut"].ctypes.data, seg["seg_cut"].ctypes.data,
+                                 seg["seg_src"].ctypes.data, ctypes.byref(nn), ctypes.byref(ns),
+                                 ctypes.byref(used))
+    if st != PS_OK:
+        raise PsError(st, "ps_build_bfs_tree")
+    out = {k: v[:nn.value].copy() for k, v in arr.items()}
+    out.update({k: v[:ns.value].copy() for k, v in seg.items()})
+    out["cuts_used"] = used.value
+    return out
+
+
+def ps_predictive_allocation(acc, rej, candidate, h_acc, budget: int) -> tuple[float, np.ndarray]:
+    """The eq. (19) dynamic program (host; see include/ps.h)."""
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    rej = np.ascontiguousarray(rej, dtype=np.int32)
+    cand = np.ascontiguousarray(candidate, dtype=np.uint8)
+    h = np.ascontiguousarray(h_acc, dtype=np.float64)
+    n = int(acc.shape[0])
+    sel = np.zeros(n, np.uint8)
+    val = ctypes.c_double()
+    st = lib().ps_predictive_allocation(n, acc.ctypes.data, rej.ctypes.data, cand.ctypes.data,
+                                        h.ctypes.data, int(budget), ctypes.byref(val),
+                                        sel.ctypes.data)
+    if st != PS_OK:
+        raise PsError(st, "ps_predictive_allocation")
+    return val.value, sel.astype(bool)
+
+
+def ps_midpoint_branch_probability(p_accept: float, p_reject: float) -> float:
+    return float(lib().ps_midpoint_branch_probability(float(p_accept), float(p_reject)))
 
 
 def ps_validate_subtree(batch: PsSubtreeBatch | None, tree: PsTree | None) -> tuple[int, str]:
