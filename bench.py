@@ -40,8 +40,8 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
 # ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
-NCU_TRAFFIC = {"source_sha1": "2aa40774de59b34f755bd126f39f0420ec1845b8",
-               "bytes_per_launch": 4160403712 + 3733504}
+NCU_TRAFFIC = {"source_sha1": "2489655186311b1379c1cc5f15be3c9a7ce04ecd",
+               "bytes_per_launch": 4160381952 + 3832576}
 
 
 def log(*a):
@@ -303,6 +303,9 @@ def main():
     k1a, k1b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k1c, k1d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ent_rows = torch.empty(w.n_rows, dtype=torch.float64, device=dev)
+    mt_taus = [0.25, 0.5, 1.0]          # MultiTryMH candidate temperatures
+    mt_lq = torch.empty((len(mt_taus), w.n_rows), dtype=torch.float64, device=dev)
+    k1e, k1f = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -329,6 +332,12 @@ def main():
             ps.ps_score_rows(d.batch, d.t["lp0"], d.t["lq"], d.t["status"], d.workspace,
                              stream, entropy=ent_rows)
         k1d.record(stream)
+        # and the multi-temperature variant (log q at all three temperatures)
+        k1e.record(stream)
+        for _ in range(args.steps):
+            ps.ps_score_rows_multi(d.batch, mt_taus, d.t["lp0"], mt_lq, d.t["status"],
+                                   d.workspace, stream)
+        k1f.record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
     if ws > 1:
@@ -337,6 +346,9 @@ def main():
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
     k1_avg = k1a.elapsed_time(k1b) / args.steps
     k1_ent_avg = k1c.elapsed_time(k1d) / args.steps
+    k1_mt_avg = k1e.elapsed_time(k1f) / args.steps
+    st = int(d.t["status"].item())
+    assert st == 0, ps.dev_status_names(st)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(units_per_step, ws, args.steps, total_ms)
 
@@ -368,6 +380,8 @@ def main():
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
         "with_entropy": {"kernel_ms": k1_ent_avg,
                          "logits_GBps": logits_bytes / (k1_ent_avg / 1e3) / 1e9},
+        "multi_temperature": {"taus": mt_taus, "kernel_ms": k1_mt_avg,
+                              "logits_GBps": logits_bytes / (k1_mt_avg / 1e3) / 1e9},
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,

@@ -55,7 +55,7 @@ typedef enum {
     PS_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, bad parameter */
     PS_ERR_INFEASIBLE = 2,    /* a request violates Condition 1 (c_i > c_src) */
     PS_ERR_BAD_TREE = 3,      /* tree arrays inconsistent (child/segment ids, cycles) */
-    PS_ERR_UNSUPPORTED = 4,   /* dtype or device not supported */
+    PS_ERR_UNSUPPORTED = 4,   /* dtype, device or temperature set not supported */
     PS_ERR_CUDA = 5,          /* a CUDA runtime call failed */
     PS_ERR_TIMEOUT = 6,       /* reserved: device waits report PS_DEV_TIMEOUT */
     PS_ERR_WORKSPACE = 7      /* workspace null, misaligned or too small */
@@ -208,6 +208,30 @@ ps_status ps_score_rows(const ps_subtree_batch *batch, double *lp0, double *lq, 
                         void *cuda_stream);
 ps_status ps_assemble_subtree(const ps_subtree_batch *batch, const double *lp0,
                               const double *lq, const ps_score_out *out, void *cuda_stream);
+
+/*
+ * Multi-temperature row scoring (MultiTryMH, as the PreSTO pages describe it
+ * in section 5.1 and Appendix D.4, Table 6(a): each candidate suffix is drawn
+ * at a temperature from {0.25, 0.5, 1.0}, and the sequential sampler rescores
+ * every candidate at all of them).  One pass over each row gives log p0 of the
+ * row's token and log q_tau of it for every tau in taus[0..n_taus-1]:
+ *     lq[k * n_rows + r] = log softmax(l_r / taus[k])[tok_r].
+ * The multiple-try Metropolis update itself is not part of this library.
+ *
+ * taus      host array of n_taus temperatures, 1 <= n_taus <= 4, each with 1/tau
+ *           exactly 1, 2, 4 or 8 (0.25, 0.5 and 1.0 qualify); anything else
+ *           returns PS_ERR_UNSUPPORTED (use ps_score_rows once per tau).
+ * lp0       [n_rows] device float64, required.
+ * lq        [n_taus][n_rows] device float64, required.
+ * entropy   [n_rows] device float64 or NULL, as for ps_score_rows.
+ * The batch is read as by ps_score_rows except that batch->tau is ignored
+ * (it must still be a positive finite number).  status, workspace and stream
+ * as for ps_score_rows; errors and device status bits are the same.
+ */
+ps_status ps_score_rows_multi(const ps_subtree_batch *batch, const double *taus,
+                              int32_t n_taus, double *lp0, double *lq, double *entropy,
+                              int32_t *status, void *workspace, size_t workspace_bytes,
+                              void *cuda_stream);
 
 /*
  * Round carry-over (section 3.2 step (3): after the walk the sampler keeps the

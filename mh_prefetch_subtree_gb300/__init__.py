@@ -28,6 +28,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libps.so")
 
 PS_OK = 0
+PS_ERR_INVALID_ARG, PS_ERR_INFEASIBLE, PS_ERR_BAD_TREE, PS_ERR_UNSUPPORTED = 1, 2, 3, 4
+PS_ERR_CUDA, PS_ERR_TIMEOUT, PS_ERR_WORKSPACE = 5, 6, 7
 PS_BF16, PS_F32 = 0, 1
 PS_DEV_BITS = {
     0x01: "BAD_TOKEN", 0x02: "NONFINITE", 0x04: "INFEASIBLE", 0x08: "BAD_TREE",
@@ -97,6 +99,10 @@ def lib() -> ctypes.CDLL:
         L.ps_score_rows.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
         L.ps_score_rows.restype = ctypes.c_int
+        L.ps_score_rows_multi.argtypes = [ctypes.POINTER(PsSubtreeBatch),
+                                          ctypes.POINTER(ctypes.c_double), ctypes.c_int32,
+                                          _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.ps_score_rows_multi.restype = ctypes.c_int
         L.ps_assemble_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), _vp, _vp,
                                           ctypes.POINTER(PsScoreOut), _vp]
         L.ps_assemble_subtree.restype = ctypes.c_int
@@ -180,6 +186,28 @@ def ps_score_rows(batch: PsSubtreeBatch, lp0: torch.Tensor, lq: torch.Tensor,
                              _ptr(status), _ptr(workspace), ws_bytes, _stream(stream, workspace))
     if check and st != PS_OK:
         raise PsError(st, "ps_score_rows")
+    return st
+
+
+def ps_score_rows_multi(batch: PsSubtreeBatch, taus, lp0: torch.Tensor, lq: torch.Tensor,
+                        status: torch.Tensor, workspace: torch.Tensor, stream=None,
+                        check: bool = True, entropy: torch.Tensor | None = None) -> int:
+    """log p0 and log q_tau for several temperatures in one pass (each 1/tau
+    in {1, 2, 4, 8}); lq is [len(taus), n_rows]."""
+    taus = [float(t) for t in taus]
+    _need(lp0, torch.float64, "lp0")
+    _need(lq, torch.float64, "lq")
+    _need(entropy, torch.float64, "entropy", optional=True)
+    _need(status, torch.int32, "status")
+    if len(lq.shape) != 2 or lq.shape[0] != len(taus) or lq.shape[1] != lp0.shape[0]:
+        raise ValueError("lq must be [len(taus), n_rows]")
+    arr = (ctypes.c_double * max(1, len(taus)))(*taus)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().ps_score_rows_multi(ctypes.byref(batch), arr, len(taus), _ptr(lp0), _ptr(lq),
+                                   _ptr(entropy), _ptr(status), _ptr(workspace), ws_bytes,
+                                   _stream(stream, workspace))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_score_rows_multi")
     return st
 
 

@@ -127,18 +127,22 @@ size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
     return ws_layout(batch->n_rows).total;
 }
 
-ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, double *entropy,
-                        int32_t *status, void *workspace, size_t workspace_bytes,
-                        void *cuda_stream) {
-    ps_status st = check_batch_host(b);
-    if (st != PS_OK) return st;
-    if (!lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Shared launch of the row kernel.  npow/g select the tau path; for the
+// multi-temperature mode (npow == 16) taus_pow/n_taus/lq_multi replace lq.
+ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
+                            double *entropy, int32_t *status, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream, int32_t npow, float g,
+                            const int32_t *tau_pow, int32_t n_taus, double *lq_multi) {
     const WsLayout wl = ws_layout(b->n_rows);
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
         return PS_ERR_WORKSPACE;
     if (b->n_rows == 0) return PS_OK;
     int sms = 0;
-    st = device_of(b->logits, &sms);
+    ps_status st = device_of(b->logits, &sms);
     if (st != PS_OK) return st;
     cudaStream_t stream = (cudaStream_t)cuda_stream;
     uint8_t *ws = (uint8_t *)workspace;
@@ -159,8 +163,11 @@ ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, doub
     if (warps > ps::kMaxWarps) warps = ps::kMaxWarps;
     if (warps > p.n_chunks) warps = p.n_chunks;
     p.n_vwarps = (int32_t)warps;
-    p.npow = integer_power(b->tau);
-    p.g = (float)(1.0 / b->tau);
+    p.npow = npow;
+    p.g = g;
+    p.n_taus = n_taus;
+    for (int k = 0; k < 4; ++k) p.tau_pow[k] = (tau_pow && k < n_taus) ? tau_pow[k] : 0;
+    p.lq_multi = lq_multi;
     p.lp0 = lp0;
     p.lq = lq;
     p.entropy = entropy;
@@ -171,6 +178,38 @@ ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, doub
     st = map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
     if (st != PS_OK) return st;
     return map_cuda(ps::launch_score_rows(p, n_ctas, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+ps_status ps_score_rows(const ps_subtree_batch *b, double *lp0, double *lq, double *entropy,
+                        int32_t *status, void *workspace, size_t workspace_bytes,
+                        void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
+    return score_rows_launch(b, lp0, lq, entropy, status, workspace, workspace_bytes,
+                             cuda_stream, integer_power(b->tau), (float)(1.0 / b->tau),
+                             nullptr, 0, nullptr);
+}
+
+ps_status ps_score_rows_multi(const ps_subtree_batch *b, const double *taus, int32_t n_taus,
+                              double *lp0, double *lq, double *entropy, int32_t *status,
+                              void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (n_taus < 1 || n_taus > 4) return PS_ERR_UNSUPPORTED;
+    if (!taus || !lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
+    int32_t pw[4];
+    for (int32_t k = 0; k < n_taus; ++k) {
+        if (!(taus[k] > 0.0) || !isfinite(taus[k])) return PS_ERR_INVALID_ARG;
+        pw[k] = integer_power(taus[k]);
+        if (pw[k] == 0) return PS_ERR_UNSUPPORTED;
+    }
+    return score_rows_launch(b, lp0, nullptr, entropy, status, workspace, workspace_bytes,
+                             cuda_stream, 16, 1.f, pw, n_taus, lq);
 }
 
 ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, const double *lq,

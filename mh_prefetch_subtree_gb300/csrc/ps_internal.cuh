@@ -25,10 +25,12 @@ constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
 struct __align__(16) RowPart {
     float R;
     float s1;
-    float st;
+    float st;       // tau sum (multi-temperature: the sum of 2^(2y))
     float ltok;
     float y1;
-    float pad[3];
+    float st1;      // multi-temperature: sums of 2^(4y) and 2^(8y)
+    float st2;
+    float pad;
 };
 
 struct RowsParams {
@@ -44,8 +46,12 @@ struct RowsParams {
     int32_t cpr;                // chunks per row
     int64_t n_chunks;           // n_rows * cpr
     int32_t n_vwarps;           // warps that own a non-empty chunk range
-    int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; else 0
+    int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; 16: several temperatures
+                                // with 1/tau in {1, 2, 4, 8} (tau_pow); else 0
     float g;                    // 1/tau in float
+    int32_t n_taus;             // multi-temperature: number of temperatures (1..4)
+    int32_t tau_pow[4];         // multi-temperature: 1/tau of each
+    double *lq_multi;           // multi-temperature: [n_taus][n_rows]
     double *lp0;
     double *lq;
     double *entropy;            // optional: entropy of p0 per row

@@ -17,7 +17,8 @@
 // lane starts with R = -inf; a chunk whose sums overflow (or are NaN) takes a
 // slow path that raises R to the chunk's maximum and rescales.  When 1/tau is
 // 1, 2, 4 or 8 the tau exponential is the first one squared, so each logit
-// costs one MUFU ex2.
+// costs one MUFU ex2; the same squaring chain serves up to four such
+// temperatures in one pass (multi-temperature scoring).
 //
 // Data movement.  The rows are cut into chunks of one stage (the last chunk of
 // a row may be shorter).  The chunk sequence of all rows is split into
@@ -91,51 +92,73 @@ __device__ __forceinline__ float max_nan_f32(float a, float b) {
     return d;
 }
 
+// NP == kAllPowers: one pass serves several temperatures whose 1/tau is 1, 2,
+// 4 or 8 (the MultiTryMH set {0.25, 0.5, 1} among them): from 2^y the powers
+// 2^(2y), 2^(4y), 2^(8y) are squares, and all three sums are kept.
+constexpr int kAllPowers = 16;
+
+template <int NP>
+__host__ __device__ constexpr int n_tau_sums() { return NP == kAllPowers ? 3 : 1; }
+
 // Running sums of one lane (or one merged part) relative to reference R.
+// st[k] is the tau sum (for kAllPowers: the sums of 2^(2y), 2^(4y), 2^(8y)).
 struct Acc {
     float R;
     float s1;
-    float st;
+    float st[3];
     float y1;
 };
 
-__device__ __forceinline__ Acc acc_empty() { return Acc{-INFINITY, 0.f, 0.f, 0.f}; }
+__device__ __forceinline__ Acc acc_empty() { return Acc{-INFINITY, 0.f, {0.f, 0.f, 0.f}, 0.f}; }
 
-// One pair of logits: accumulate 2^x into a1, 2^(g x) into at and 2^x x into ay.
+// One pair of logits: accumulate 2^x into a1, 2^(g x) into at[0] (or the three
+// power sums into at[0..2]) and 2^x x into ay.
 template <int NP, bool ENT>
 __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2, float2 &a1,
-                                      float2 &at, float2 &ay) {
+                                      float2 (&at)[3], float2 &ay) {
     const float2 x = __ffma2_rn(v, L2, nR2);
     const float2 e = make_float2(ex2(x.x), ex2(x.y));
     a1 = __fadd2_rn(a1, e);
     if constexpr (ENT) ay = __ffma2_rn(e, x, ay);
     if constexpr (NP == 2) {
-        at = __fadd2_rn(at, __fmul2_rn(e, e));
+        at[0] = __fadd2_rn(at[0], __fmul2_rn(e, e));
     } else if constexpr (NP == 4) {
         const float2 e2 = __fmul2_rn(e, e);
-        at = __fadd2_rn(at, __fmul2_rn(e2, e2));
+        at[0] = __fadd2_rn(at[0], __fmul2_rn(e2, e2));
     } else if constexpr (NP == 8) {
         const float2 e2 = __fmul2_rn(e, e);
         const float2 e4 = __fmul2_rn(e2, e2);
-        at = __fadd2_rn(at, __fmul2_rn(e4, e4));
+        at[0] = __fadd2_rn(at[0], __fmul2_rn(e4, e4));
+    } else if constexpr (NP == kAllPowers) {
+        const float2 e2 = __fmul2_rn(e, e);
+        const float2 e4 = __fmul2_rn(e2, e2);
+        at[0] = __fadd2_rn(at[0], e2);
+        at[1] = __fadd2_rn(at[1], e4);
+        at[2] = __fadd2_rn(at[2], __fmul2_rn(e4, e4));
     } else if constexpr (NP == 0) {
         const float2 xt = __fmul2_rn(x, G2);
-        at = __fadd2_rn(at, make_float2(ex2(xt.x), ex2(xt.y)));
+        at[0] = __fadd2_rn(at[0], make_float2(ex2(xt.x), ex2(xt.y)));
     }
 }
 
-// Sums of one lane's VPL vectors relative to reference R.
+__device__ __forceinline__ float hsum4(const float2 (&a)[4]) {
+    const float2 s01 = __fadd2_rn(a[0], a[1]), s23 = __fadd2_rn(a[2], a[3]);
+    const float2 s = __fadd2_rn(s01, s23);
+    return s.x + s.y;
+}
+
+// Sums of one lane's VPL vectors relative to reference R: c1, ct[0..NS-1], cy.
 template <int DT, int NP, bool ENT, int VPL>
 __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g, float &c1,
-                                         float &ct, float &cy) {
+                                         float (&ct)[3], float &cy) {
     const float2 L2 = make_float2(kLog2e, kLog2e);
     const float2 nR2 = make_float2(-R, -R);
     const float2 G2 = make_float2(g, g);
-    float2 a1[4], at[4], ay[4];
+    float2 a1[4], at[4][3], ay[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         a1[j] = make_float2(0.f, 0.f);
-        at[j] = make_float2(0.f, 0.f);
+        at[j][0] = at[j][1] = at[j][2] = make_float2(0.f, 0.f);
         ay[j] = make_float2(0.f, 0.f);
     }
 #pragma unroll
@@ -162,29 +185,24 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
                            at[(i & 1) * 2 + 1], ay[(i & 1) * 2 + 1]);
         }
     }
-    const float2 s01 = __fadd2_rn(a1[0], a1[1]), s23 = __fadd2_rn(a1[2], a1[3]);
-    const float2 s = __fadd2_rn(s01, s23);
-    c1 = s.x + s.y;
+    c1 = hsum4(a1);
     if constexpr (NP == 1) {
-        ct = c1;
+        ct[0] = c1;
     } else {
-        const float2 t01 = __fadd2_rn(at[0], at[1]), t23 = __fadd2_rn(at[2], at[3]);
-        const float2 t = __fadd2_rn(t01, t23);
-        ct = t.x + t.y;
+#pragma unroll
+        for (int k = 0; k < n_tau_sums<NP>(); ++k) {
+            const float2 t[4] = {at[0][k], at[1][k], at[2][k], at[3][k]};
+            ct[k] = hsum4(t);
+        }
     }
-    if constexpr (ENT) {
-        const float2 y01 = __fadd2_rn(ay[0], ay[1]), y23 = __fadd2_rn(ay[2], ay[3]);
-        const float2 y = __fadd2_rn(y01, y23);
-        cy = y.x + y.y;
-    } else {
-        cy = 0.f;
-    }
+    cy = ENT ? hsum4(ay) : 0.f;
 }
 
-// Rescale factor for the tau sums when the reference moves by d (log2 units).
+// Rescale factor of tau sum k when the reference moves by d (log2 units).
 template <int NP>
-__device__ __forceinline__ float tau_scale(float d, float g) {
+__device__ __forceinline__ float tau_scale(float d, float g, int k) {
     if constexpr (NP == 0) return ex2(d * g);
+    else if constexpr (NP == kAllPowers) return ex2(d * (float)(2 << k));
     else return ex2(d * (float)NP);
 }
 
@@ -200,7 +218,10 @@ __device__ __forceinline__ Acc rebase(Acc a, float Rn, float g) {
     const float f = ex2(d);
     if constexpr (ENT) a.y1 = f * fmaf(d, a.s1, a.y1);
     a.s1 *= f;
-    if constexpr (NP != 1) a.st *= tau_scale<NP>(d, g);
+    if constexpr (NP != 1) {
+#pragma unroll
+        for (int k = 0; k < n_tau_sums<NP>(); ++k) a.st[k] *= tau_scale<NP>(d, g, k);
+    }
     a.R = Rn;
     return a;
 }
@@ -220,6 +241,23 @@ __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
         const int idx = lane + 32 * i;
         q[i] = idx < nvec ? v4[idx] : make_uint4(ni, ni, ni, ni);
     }
+}
+
+// Adds a chunk's sums to the running ones.
+template <int NP, bool ENT>
+__device__ __forceinline__ void add_chunk(Acc &a, float c1, const float (&ct)[3], float cy) {
+    a.s1 += c1;
+    if constexpr (NP != 1) {
+#pragma unroll
+        for (int k = 0; k < n_tau_sums<NP>(); ++k) a.st[k] += ct[k];
+    }
+    if constexpr (ENT) a.y1 += cy;
+}
+
+// The largest of a chunk's sums (the one that overflows first).
+template <int NP>
+__device__ __forceinline__ float chunk_peak(float c1, const float (&ct)[3]) {
+    return fmaxf(c1, ct[n_tau_sums<NP>() - 1]);
 }
 
 // Rare path: the chunk's sums overflowed or were NaN (always the case for a
@@ -251,17 +289,16 @@ __device__ __noinline__ Acc slow_chunk(const uint4 *v4, int nvec, int lane, floa
     }
     if (nan_seen) {
         const float qn = __int_as_float(0x7fc00000);
-        a.s1 = a.st = a.y1 = qn;
+        a.s1 = a.y1 = qn;
+        a.st[0] = a.st[1] = a.st[2] = qn;
         return a;
     }
     const float Rn = fmaxf(a.R, m * kLog2e);
     if (Rn == -INFINITY) return a;     // only -inf so far: nothing to add
     if (Rn > a.R) a = rebase<NP, ENT>(a, Rn, g);
-    float c1, ct, cy;
+    float c1, ct[3], cy;
     sum_vecs<DT, NP, ENT, VPL>(q, a.R, g, c1, ct, cy);
-    a.s1 += c1;
-    if constexpr (NP != 1) a.st += ct;
-    if constexpr (ENT) a.y1 += cy;
+    add_chunk<NP, ENT>(a, c1, ct, cy);
     return a;
 }
 
@@ -271,15 +308,16 @@ __device__ __forceinline__ Acc merge_part(Acc a, Acc b, float g) {
     const float M = fmaxf(a.R, b.R);
     if (M == -INFINITY) {              // both parts saw only -inf logits
         a.s1 += b.s1;                  // keeps a NaN poison, else 0
-        a.st += b.st;
+        a.st[0] += b.st[0];
+        a.st[1] += b.st[1];
+        a.st[2] += b.st[2];
         a.y1 += b.y1;
         return a;
     }
     a = rebase<NP, ENT>(a, M, g);
     b = rebase<NP, ENT>(b, M, g);
-    a.s1 += b.s1;
-    if constexpr (NP != 1) a.st += b.st;
-    if constexpr (ENT) a.y1 += b.y1;
+    const float z[3] = {b.st[0], b.st[1], b.st[2]};
+    add_chunk<NP, ENT>(a, b.s1, z, b.y1);
     return a;
 }
 
@@ -290,7 +328,10 @@ __device__ __forceinline__ Acc warp_merge(Acc a, float g) {
         Acc b;
         b.R = __shfl_xor_sync(0xffffffffu, a.R, off);
         b.s1 = __shfl_xor_sync(0xffffffffu, a.s1, off);
-        b.st = (NP != 1) ? __shfl_xor_sync(0xffffffffu, a.st, off) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            b.st[k] = (NP != 1 && k < n_tau_sums<NP>())
+                          ? __shfl_xor_sync(0xffffffffu, a.st[k], off) : 0.f;
         b.y1 = ENT ? __shfl_xor_sync(0xffffffffu, a.y1, off) : 0.f;
         a = merge_part<NP, ENT>(a, b, g);
     }
@@ -323,26 +364,40 @@ __device__ double entropy_nats(double s1, double y1, double t) {
 
 template <int NP, bool ENT>
 __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bool bad) {
-    double o0, oq, h = 0.0;
+    double o0, oq = 0.0, h = 0.0;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
+    if constexpr (NP == 1) a.st[0] = a.s1;
+    bool nonfinite = false;
     if (bad || __float_as_uint(lt) == kAbsent) {
         o0 = oq = h = qnan;
+        nonfinite = true;          // already flagged (token or row index)
+        if constexpr (NP == kAllPowers)
+            for (int k = 0; k < p.n_taus; ++k) p.lq_multi[(int64_t)k * p.n_rows + r] = qnan;
     } else {
-        if constexpr (NP == 1) a.st = a.s1;
         const float t = fmaf(lt, kLog2e, -a.R);
-        const bool nonfinite = (lt != lt) || (lt == INFINITY) || (a.R != a.R) ||
-                               (a.s1 != a.s1) || (a.st != a.st) || (a.R == INFINITY) ||
-                               (t != t) || (ENT && (a.y1 != a.y1));
+        nonfinite = (lt != lt) || (lt == INFINITY) || (a.R != a.R) || (a.s1 != a.s1) ||
+                    (a.st[0] != a.st[0]) || (a.st[n_tau_sums<NP>() - 1] !=
+                                             a.st[n_tau_sums<NP>() - 1]) ||
+                    (a.R == INFINITY) || (t != t) || (ENT && (a.y1 != a.y1));
         if (nonfinite) {
             set_status(p.status, PS_DEV_NONFINITE);
             o0 = oq = h = qnan;
+            if constexpr (NP == kAllPowers)
+                for (int k = 0; k < p.n_taus; ++k) p.lq_multi[(int64_t)k * p.n_rows + r] = qnan;
         } else {
             o0 = neg_log1p_exp2(a.s1 > 0.f ? log2f(a.s1) - t : -INFINITY);
             if constexpr (NP == 1) {
                 oq = o0;
+            } else if constexpr (NP == kAllPowers) {
+                for (int k = 0; k < p.n_taus; ++k) {
+                    const int pw = p.tau_pow[k];           // 1/tau: 1, 2, 4 or 8
+                    const float sk = pw == 1 ? a.s1 : (pw == 2 ? a.st[0] : (pw == 4 ? a.st[1] : a.st[2]));
+                    p.lq_multi[(int64_t)k * p.n_rows + r] =
+                        neg_log1p_exp2(sk > 0.f ? log2f(sk) - t * (float)pw : -INFINITY);
+                }
             } else {
                 const float gt = (NP == 0) ? t * p.g : t * (float)NP;
-                oq = neg_log1p_exp2(a.st > 0.f ? log2f(a.st) - gt : -INFINITY);
+                oq = neg_log1p_exp2(a.st[0] > 0.f ? log2f(a.st[0]) - gt : -INFINITY);
             }
             if constexpr (ENT) {
                 // a token logit of -inf has no mass: t = -inf leaves it out
@@ -352,7 +407,7 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
         }
     }
     p.lp0[r] = o0;
-    p.lq[r] = oq;
+    if constexpr (NP != kAllPowers) p.lq[r] = oq;
     if constexpr (ENT) p.entropy[r] = h;
 }
 
@@ -513,12 +568,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             const int nvec = (int)(bytes >> 4);
             uint4 q[kVecPerLane];
             load_vecs<DT, kVecPerLane>(v4, nvec, lane, q);
-            float c1, ct, cy;
+            float c1, ct[3], cy;
             sum_vecs<DT, NP, ENT, kVecPerLane>(q, acc.R, g, c1, ct, cy);
-            if (fmaxf(c1, ct) <= kLimit) {
-                acc.s1 += c1;
-                if constexpr (NP != 1) acc.st += ct;
-                if constexpr (ENT) acc.y1 += cy;
+            if (chunk_peak<NP>(c1, ct) <= kLimit) {
+                add_chunk<NP, ENT>(acc, c1, ct, cy);
             } else {
                 acc = slow_chunk<DT, NP, ENT, kVecPerLane>(v4, nvec, lane, g, acc);
             }
@@ -542,10 +595,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
                     RowPart part;
                     part.R = acc.R;
                     part.s1 = acc.s1;
-                    part.st = acc.st;
+                    part.st = acc.st[0];
                     part.ltok = lt;
                     part.y1 = acc.y1;
-                    part.pad[0] = part.pad[1] = part.pad[2] = 0.f;
+                    part.st1 = acc.st[1];
+                    part.st2 = acc.st[2];
+                    part.pad = 0.f;
                     p.parts[slot] = part;
                     __threadfence();
                     const int old = atomicAdd(p.counters + owner, 1);
@@ -561,8 +616,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
                         const int64_t su =
                             (row == range_begin(u, C, W) / cpr) ? 2 * u : 2 * u + 1;
                         const float4 pv = __ldcg(reinterpret_cast<const float4 *>(p.parts + su));
-                        const float py = __ldcg(&p.parts[su].y1);
-                        m = merge_part<NP, ENT>(m, Acc{pv.x, pv.y, pv.z, py}, g);
+                        const float4 pw =
+                            __ldcg(reinterpret_cast<const float4 *>(p.parts + su) + 1);
+                        m = merge_part<NP, ENT>(m, Acc{pv.x, pv.y, {pv.z, pw.y, pw.z}, pw.x}, g);
                         if (__float_as_uint(pv.w) != kAbsent) ltm = pv.w;
                     }
                     m = warp_merge<NP, ENT>(m, g);
@@ -611,6 +667,7 @@ cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
         case 2: return launch_t<DT, 2, ENT>(p, n_ctas, stream);
         case 4: return launch_t<DT, 4, ENT>(p, n_ctas, stream);
         case 8: return launch_t<DT, 8, ENT>(p, n_ctas, stream);
+        case kAllPowers: return launch_t<DT, kAllPowers, ENT>(p, n_ctas, stream);
         default: return launch_t<DT, 0, ENT>(p, n_ctas, stream);
     }
 }

@@ -9,6 +9,8 @@ Sampling" (arXiv 2610.13171) in float64, step by step and without shortcuts:
 
 * ``row_logprobs``      per-token log p0 and log q_tau from the same logits
                         (Appendix B.1, last paragraph; Appendix D.3), in C;
+                        called once per temperature it is also the oracle of
+                        multi-temperature scoring (MultiTryMH, Table 6(a));
 * ``materialize``       the full state of every tree node as an explicit
                         position -> row map (section 3.2 step (1); a rejection
                         child keeps its parent's state; Condition 1);

@@ -162,3 +162,30 @@ def test_host_argument_checks_need_no_gpu():
     b.dtype = 7
     assert ps.ps_score_subtree(b, out, ws, check=False, stream=0) == 4
     assert ps.ps_score_workspace_bytes(b) > 0
+
+
+def test_multi_temperature_host_checks_need_no_gpu():
+    import torch
+    lay = assemble_layout([example5_tree(8, 5, 2)])
+    b, _ = _host(lay)
+    logits = torch.zeros(lay.n_rows, 64, dtype=torch.bfloat16)
+    toks = torch.zeros(lay.n_rows, dtype=torch.int32)
+    b.logits = logits.data_ptr()
+    b.tokens = toks.data_ptr()
+    lp0 = torch.zeros(lay.n_rows, dtype=torch.float64)
+    status = torch.zeros(1, dtype=torch.int32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+
+    def call(taus):
+        lq = torch.zeros(len(taus), lay.n_rows, dtype=torch.float64)
+        return ps.ps_score_rows_multi(b, taus, lp0, lq, status, ws, check=False, stream=0)
+
+    # 1/tau outside {1, 2, 4, 8}, or more than four temperatures: unsupported
+    assert call([0.25, 0.3]) == 4
+    assert call([1.0, 0.5, 0.25, 0.125, 1.0]) == 4
+    assert call([]) == 4
+    # a temperature that is not a positive finite number: invalid argument
+    assert call([0.25, -0.5]) == 1
+    assert call([float("nan")]) == 1
+    # supported temperatures pass the checks and stop at the workspace size
+    assert call([0.25, 0.5, 1.0]) == 7
