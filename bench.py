@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is abse
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
 # ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
 NCU_TRAFFIC = {"source_sha1": "2489655186311b1379c1cc5f15be3c9a7ce04ecd",
-               "bytes_per_launch": 4160381952 + 3832576}
+               "bytes_per_launch": 4160381952 + 3832576, "config": 2}
 
 
 def log(*a):
@@ -360,8 +360,9 @@ def main():
     peak, peak_src = peaks()
     achieved = alg_bytes_k1 / (k1_avg / 1e3) / 1e9
     traffic = None
-    if NCU_TRAFFIC["source_sha1"] == kernel_source_sha1():
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    if (NCU_TRAFFIC["source_sha1"] == kernel_source_sha1() and args.config == NCU_TRAFFIC["config"]
+            and args.n_pf is None):
+        traffic = NCU_TRAFFIC["bytes_per_launch"]     # captured on this workload
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

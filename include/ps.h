@@ -418,6 +418,20 @@ ps_status ps_predictive_allocation(int32_t n_nodes, const int32_t *acc, const in
 double ps_midpoint_branch_probability(double p_accept, double p_reject);
 
 /* Static text for a status code. */
+/*
+ * Diagnostic with no counterpart in the PreSTO pages: checks on the device the
+ * bounded wait that every bulk-copy wait of the scoring kernel uses.  One warp
+ * waits on a shared-memory mbarrier that nothing completes; after limit_ns of
+ * wall time (or a fixed poll count) the wait gives up and PS_DEV_TIMEOUT is
+ * OR-ed into *status, and the kernel returns, leaving the context usable.
+ * This lets a caller or a test see the timeout path work without faulting or
+ * hanging the GPU.
+ *
+ * limit_ns  1,000 .. 2,000,000,000 (1 us .. 2 s), else PS_ERR_INVALID_ARG.
+ * status    device int32 word, required.
+ */
+ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status, void *cuda_stream);
+
 const char *ps_status_string(ps_status status);
 
 /* Library version string. */

@@ -128,6 +128,8 @@ def lib() -> ctypes.CDLL:
         L.ps_validate_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsTree),
                                           ctypes.c_char_p, ctypes.c_size_t]
         L.ps_validate_subtree.restype = ctypes.c_int
+        L.ps_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp, _vp]
+        L.ps_selftest_wait_timeout.restype = ctypes.c_int
         L.ps_status_string.argtypes = [ctypes.c_int]
         L.ps_status_string.restype = ctypes.c_char_p
         L.ps_version.argtypes = []
@@ -208,6 +210,17 @@ def ps_score_rows_multi(batch: PsSubtreeBatch, taus, lp0: torch.Tensor, lq: torc
                                    _stream(stream, workspace))
     if check and st != PS_OK:
         raise PsError(st, "ps_score_rows_multi")
+    return st
+
+
+def ps_selftest_wait_timeout(limit_ns: int, status: torch.Tensor, stream=None,
+                             check: bool = True) -> int:
+    """Diagnostic: a device wait that nothing completes gives up after limit_ns
+    and sets PS_DEV_TIMEOUT in status (see include/ps.h)."""
+    _need(status, torch.int32, "status")
+    st = lib().ps_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream(stream, status))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_selftest_wait_timeout")
     return st
 
 

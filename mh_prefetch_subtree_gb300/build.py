@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libps.so")
-SOURCES = ["ps_score_rows.cu", "ps_assemble.cu", "ps_walk.cu", "ps_carry.cu", "ps_tree.cu", "ps_api.cu"]
+SOURCES = ["ps_score_rows.cu", "ps_assemble.cu", "ps_walk.cu", "ps_carry.cu", "ps_tree.cu", "ps_selftest.cu",
+           "ps_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                  "-I", os.path.join(ROOT, "include")]

@@ -202,14 +202,16 @@ ps_status ps_score_rows_multi(const ps_subtree_batch *b, const double *taus, int
     if (st != PS_OK) return st;
     if (n_taus < 1 || n_taus > 4) return PS_ERR_UNSUPPORTED;
     if (!taus || !lp0 || !lq || !status) return PS_ERR_INVALID_ARG;
-    int32_t pw[4];
+    int32_t pw[4], top = 1;
     for (int32_t k = 0; k < n_taus; ++k) {
         if (!(taus[k] > 0.0) || !isfinite(taus[k])) return PS_ERR_INVALID_ARG;
         pw[k] = integer_power(taus[k]);
         if (pw[k] == 0) return PS_ERR_UNSUPPORTED;
+        if (pw[k] > top) top = pw[k];
     }
+    // the kernel keeps the power sums up to 2^(4y), or up to 2^(8y) when needed
     return score_rows_launch(b, lp0, nullptr, entropy, status, workspace, workspace_bytes,
-                             cuda_stream, 16, 1.f, pw, n_taus, lq);
+                             cuda_stream, top == 8 ? 16 : 17, 1.f, pw, n_taus, lq);
 }
 
 ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, const double *lq,
@@ -523,7 +525,16 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
 }
 
-extern "C" ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
+extern "C" ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status, void *cuda_stream) {
+    if (limit_ns < 1000ull || limit_ns > 2000000000ull) return PS_ERR_INVALID_ARG;
+    if (!status) return PS_ERR_INVALID_ARG;
+    int sms = 0;
+    ps_status st = device_of(status, &sms);
+    if (st != PS_OK) return st;
+    return map_cuda(ps::launch_wait_selftest(limit_ns, status, (cudaStream_t)cuda_stream));
+}
+
+ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
                                     void *cuda_stream) {
     if (!b || !io || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)
         return PS_ERR_INVALID_ARG;

@@ -13,9 +13,9 @@ namespace ps {
 // row chunks through a private ring of shared-memory stages filled by 1-D bulk
 // copies; see ps_score_rows.cu.
 // ---------------------------------------------------------------------------
-constexpr int kWarpsPerCta = 8;
+constexpr int kWarpsPerCta = 16;
 constexpr int kStages = 2;
-constexpr int kStageBytes = 8192;
+constexpr int kStageBytes = 4096;
 constexpr int kMaxCtas = 2048;                        // workspace sizing bound
 constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
 
@@ -46,8 +46,9 @@ struct RowsParams {
     int32_t cpr;                // chunks per row
     int64_t n_chunks;           // n_rows * cpr
     int32_t n_vwarps;           // warps that own a non-empty chunk range
-    int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; 16: several temperatures
-                                // with 1/tau in {1, 2, 4, 8} (tau_pow); else 0
+    int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; 16 (17): several
+                                // temperatures with 1/tau in {1, 2, 4, 8} ({1, 2, 4}),
+                                // listed in tau_pow; else 0
     float g;                    // 1/tau in float
     int32_t n_taus;             // multi-temperature: number of temperatures (1..4)
     int32_t tau_pow[4];         // multi-temperature: 1/tau of each
@@ -115,6 +116,8 @@ cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);
 cudaError_t launch_carry(const CarryParams &p, cudaStream_t stream);
 size_t score_rows_smem_bytes();
+// Diagnostic: a bounded wait on an mbarrier that nothing completes.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t *status, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -164,15 +167,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Bounded wait: spins on try_wait (which itself suspends for a short,
-// hardware-chosen time) and gives up after `limit_ns` of wall time.
+// hardware-chosen time) and gives up after `limit_ns` of wall time, or after
+// 2^28 polls whatever the timer says.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (uint32_t i = 1; i < (1u << 28); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
+    return false;
 }
 
 // L2 policy for data read exactly once: evict it first, so that the small

@@ -92,16 +92,23 @@ __device__ __forceinline__ float max_nan_f32(float a, float b) {
     return d;
 }
 
-// NP == kAllPowers: one pass serves several temperatures whose 1/tau is 1, 2,
-// 4 or 8 (the MultiTryMH set {0.25, 0.5, 1} among them): from 2^y the powers
-// 2^(2y), 2^(4y), 2^(8y) are squares, and all three sums are kept.
-constexpr int kAllPowers = 16;
+// NP == kAllPowers or kPowersTo4: one pass serves several temperatures whose
+// 1/tau is 1, 2, 4 or 8 (the MultiTryMH set {0.25, 0.5, 1} among them): from
+// 2^y the powers 2^(2y), 2^(4y) (and, for kAllPowers, 2^(8y)) are squares,
+// and their sums are kept side by side.
+constexpr int kAllPowers = 16;     // sums of 2^(2y), 2^(4y), 2^(8y)
+constexpr int kPowersTo4 = 17;     // sums of 2^(2y), 2^(4y)
 
 template <int NP>
-__host__ __device__ constexpr int n_tau_sums() { return NP == kAllPowers ? 3 : 1; }
+__host__ __device__ constexpr bool multi_tau() { return NP == kAllPowers || NP == kPowersTo4; }
+
+template <int NP>
+__host__ __device__ constexpr int n_tau_sums() {
+    return NP == kAllPowers ? 3 : (NP == kPowersTo4 ? 2 : 1);
+}
 
 // Running sums of one lane (or one merged part) relative to reference R.
-// st[k] is the tau sum (for kAllPowers: the sums of 2^(2y), 2^(4y), 2^(8y)).
+// st[k] is the tau sum (multi-temperature: the sum of 2^(2^(k+1) y)).
 struct Acc {
     float R;
     float s1;
@@ -129,12 +136,12 @@ __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2
         const float2 e2 = __fmul2_rn(e, e);
         const float2 e4 = __fmul2_rn(e2, e2);
         at[0] = __fadd2_rn(at[0], __fmul2_rn(e4, e4));
-    } else if constexpr (NP == kAllPowers) {
+    } else if constexpr (multi_tau<NP>()) {
         const float2 e2 = __fmul2_rn(e, e);
         const float2 e4 = __fmul2_rn(e2, e2);
         at[0] = __fadd2_rn(at[0], e2);
         at[1] = __fadd2_rn(at[1], e4);
-        at[2] = __fadd2_rn(at[2], __fmul2_rn(e4, e4));
+        if constexpr (NP == kAllPowers) at[2] = __fadd2_rn(at[2], __fmul2_rn(e4, e4));
     } else if constexpr (NP == 0) {
         const float2 xt = __fmul2_rn(x, G2);
         at[0] = __fadd2_rn(at[0], make_float2(ex2(xt.x), ex2(xt.y)));
@@ -202,7 +209,7 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
 template <int NP>
 __device__ __forceinline__ float tau_scale(float d, float g, int k) {
     if constexpr (NP == 0) return ex2(d * g);
-    else if constexpr (NP == kAllPowers) return ex2(d * (float)(2 << k));
+    else if constexpr (multi_tau<NP>()) return ex2(d * (float)(2 << k));
     else return ex2(d * (float)NP);
 }
 
@@ -262,8 +269,9 @@ __device__ __forceinline__ float chunk_peak(float c1, const float (&ct)[3]) {
 
 // Rare path: the chunk's sums overflowed or were NaN (always the case for a
 // lane's first chunk of a row, whose reference is still -inf).  Re-reads the
-// lane's vectors from shared memory, raises R to their maximum, rescales the
-// running sums and adds the chunk.
+// lane's vectors from shared memory, raises R to their maximum (for the
+// entropy variant, which calls it on all lanes at once, to the warp's
+// maximum), rescales the running sums and adds the chunk.
 template <int DT, int NP, bool ENT, int VPL>
 __device__ __noinline__ Acc slow_chunk(const uint4 *v4, int nvec, int lane, float g, Acc a) {
     uint4 q[VPL];
@@ -286,6 +294,12 @@ __device__ __noinline__ Acc slow_chunk(const uint4 *v4, int nvec, int lane, floa
                 m = fmaxf(m, v);
             }
         }
+    }
+    if constexpr (ENT) {
+        // every lane is here (the caller votes): one reference for the warp
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     }
     if (nan_seen) {
         const float qn = __int_as_float(0x7fc00000);
@@ -371,7 +385,7 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
     if (bad || __float_as_uint(lt) == kAbsent) {
         o0 = oq = h = qnan;
         nonfinite = true;          // already flagged (token or row index)
-        if constexpr (NP == kAllPowers)
+        if constexpr (multi_tau<NP>())
             for (int k = 0; k < p.n_taus; ++k) p.lq_multi[(int64_t)k * p.n_rows + r] = qnan;
     } else {
         const float t = fmaf(lt, kLog2e, -a.R);
@@ -382,13 +396,13 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
         if (nonfinite) {
             set_status(p.status, PS_DEV_NONFINITE);
             o0 = oq = h = qnan;
-            if constexpr (NP == kAllPowers)
+            if constexpr (multi_tau<NP>())
                 for (int k = 0; k < p.n_taus; ++k) p.lq_multi[(int64_t)k * p.n_rows + r] = qnan;
         } else {
             o0 = neg_log1p_exp2(a.s1 > 0.f ? log2f(a.s1) - t : -INFINITY);
             if constexpr (NP == 1) {
                 oq = o0;
-            } else if constexpr (NP == kAllPowers) {
+            } else if constexpr (multi_tau<NP>()) {
                 for (int k = 0; k < p.n_taus; ++k) {
                     const int pw = p.tau_pow[k];           // 1/tau: 1, 2, 4 or 8
                     const float sk = pw == 1 ? a.s1 : (pw == 2 ? a.st[0] : (pw == 4 ? a.st[1] : a.st[2]));
@@ -407,7 +421,7 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
         }
     }
     p.lp0[r] = o0;
-    if constexpr (NP != kAllPowers) p.lq[r] = oq;
+    if constexpr (!multi_tau<NP>()) p.lq[r] = oq;
     if constexpr (ENT) p.entropy[r] = h;
 }
 
@@ -422,6 +436,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
     static_assert(SB % 512 == 0, "a stage holds a whole number of 16-byte vectors per lane");
     constexpr int kEsz = Elem<DT>::kSize;
     constexpr int kElemsPerStage = kStageBytes / kEsz;
+    // With entropy, sum 2^y y cancels against S1 log2 S1 when one logit holds
+    // most of the mass, so its float error grows with the distance between
+    // the reference and the largest logit.  The entropy variant therefore
+    // keeps one reference for the whole warp, and a chunk in which any lane's
+    // sum exceeds the lane's element count (which needs an element above the
+    // reference) takes the slow path on all lanes, raising the reference to
+    // the chunk's maximum: the largest terms are added within log2(count) of
+    // the reference.  A warp-wide reference tracks the row's running maximum,
+    // so this happens on few chunks.
+    constexpr float kEntLimit = (float)(kVecPerLane * 16 / kEsz);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     // the next kernel (suffix sums) may be scheduled now; it waits for this
@@ -570,7 +594,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             load_vecs<DT, kVecPerLane>(v4, nvec, lane, q);
             float c1, ct[3], cy;
             sum_vecs<DT, NP, ENT, kVecPerLane>(q, acc.R, g, c1, ct, cy);
-            if (chunk_peak<NP>(c1, ct) <= kLimit) {
+            bool fast = chunk_peak<NP>(c1, ct) <= kLimit;
+            if constexpr (ENT) fast = __all_sync(0xffffffffu, fast && c1 <= kEntLimit);
+            if (fast) {
                 add_chunk<NP, ENT>(acc, c1, ct, cy);
             } else {
                 acc = slow_chunk<DT, NP, ENT, kVecPerLane>(v4, nvec, lane, g, acc);
@@ -668,6 +694,7 @@ cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
         case 4: return launch_t<DT, 4, ENT>(p, n_ctas, stream);
         case 8: return launch_t<DT, 8, ENT>(p, n_ctas, stream);
         case kAllPowers: return launch_t<DT, kAllPowers, ENT>(p, n_ctas, stream);
+        case kPowersTo4: return launch_t<DT, kPowersTo4, ENT>(p, n_ctas, stream);
         default: return launch_t<DT, 0, ENT>(p, n_ctas, stream);
     }
 }

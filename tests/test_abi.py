@@ -189,3 +189,13 @@ def test_multi_temperature_host_checks_need_no_gpu():
     assert call([float("nan")]) == 1
     # supported temperatures pass the checks and stop at the workspace size
     assert call([0.25, 0.5, 1.0]) == 7
+
+
+def test_wait_selftest_host_checks_need_no_gpu():
+    import torch
+    st = torch.zeros(1, dtype=torch.int32)
+    # limits outside 1 us .. 2 s are rejected before any CUDA call
+    assert ps.ps_selftest_wait_timeout(10, st, stream=0, check=False) == 1
+    assert ps.ps_selftest_wait_timeout(3_000_000_000, st, stream=0, check=False) == 1
+    # a host pointer is not device memory
+    assert ps.ps_selftest_wait_timeout(1_000_000, st, stream=0, check=False) == 1

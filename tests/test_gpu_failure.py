@@ -1,0 +1,42 @@
+"""Failure detection on the GPU without a fault: a bounded device wait that
+nothing completes ends with PS_DEV_TIMEOUT, and the context stays usable."""
+
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import mh_prefetch_subtree_gb300 as ps
+from synth import make_workload
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+PS_DEV_TIMEOUT = 0x20
+
+
+def setup_module(module):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ps.ps_selftest_wait_timeout(50_000_000, status)         # 50 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(status.item()) == PS_DEV_TIMEOUT
+    assert 0.045 <= dt < 5.0, dt
+    # the context is still usable: a scoring pass right after it is correct
+    w = make_workload(1, device=DEV)
+    s = H.full_parity(w)
+    assert s["lp0_max_rel"] <= H.TOK_RTOL
+    # and a second timeout on another stream reports again
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream(device=DEV)
+    ps.ps_selftest_wait_timeout(2_000_000, st2, side)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == PS_DEV_TIMEOUT

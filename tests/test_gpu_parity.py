@@ -154,6 +154,30 @@ def test_entropy_edge_cases():
     assert abs(g["entropy"][0] - np.log(V)) < 1e-4 and g["entropy"][1] == 0.0
 
 
+@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (262144, "bf16"), (4100, "f32")])
+def test_entropy_of_peaked_rows_whose_token_is_not_the_peak(V, dtype):
+    # one logit far above the rest, placed anywhere in the row (often in a late
+    # chunk), and the token elsewhere: the entropy is small and the sum of
+    # 2^y y cancels against S1 log2 S1, so this checks that the dominant term is
+    # accumulated close to the reference
+    w = _small(V, dtype, T=12, n_pf=4, n_chains=2, seed=23, kind="normal")
+    n = w.n_rows
+    rng = np.random.default_rng(24)
+    x = w.logits.clone()
+    peak = torch.from_numpy(rng.integers(0, V, n)).to(DEV)
+    margin = torch.from_numpy(rng.choice([3.0, 6.0, 10.0, 15.0, 25.0, 40.0], n)).to(DEV)
+    rows = torch.arange(n, device=DEV)
+    x[rows, peak] = (x[:, :V].float().max(dim=1).values + margin.float()).to(x.dtype)
+    tok = torch.from_numpy(rng.integers(0, V, n).astype(np.int32)).to(DEV)
+    tok = torch.where(tok.long() == peak, (tok + 1) % V, tok)
+    w.logits, w.tokens = x, tok
+    g = H.run_gpu(w)
+    o = H.run_oracle(w)
+    s = H.check_rows(g, o)
+    _report(f"peaked off-token {V} {dtype}", s)
+    assert np.median(o["entropy"]) < 0.5
+
+
 def test_masked_vocabulary():
     w = _small(151936, "bf16", T=10, n_pf=4, n_chains=2, seed=11)
     x = w.logits.clone()
