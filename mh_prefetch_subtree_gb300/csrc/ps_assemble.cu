@@ -32,37 +32,50 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
-// Adds lp0[r], lq[r] for r = r0, r0 + 256, ... < r1 into a, b, in index order;
-// the loads of up to 8 rows are issued before any of them is added.
-__device__ __forceinline__ void range_sum(const double *lp0, const double *lq, int64_t r0,
-                                          int64_t r1, double &a, double &b) {
+// A request's sums over four row ranges laid end to end in one index space:
+// range 0 (the y rows) goes to (a, b), ranges 1-3 (the x suffix) to (e, f).
+// Range k reads lp_k[o_k + j], lq_k[o_k + j] for j < n_k.  The threads stride
+// over the index space and issue the loads of up to kU indices before adding
+// any, so a request's sums usually take one round of memory latency.  Each
+// thread adds its elements in index order: the result is deterministic.
+struct Ranges {
+    const double *lp[4];
+    const double *lq[4];
+    int64_t o[4];
+    int64_t n[4];
+};
+
+__device__ __forceinline__ void ranges_sum(const Ranges &g, int tid, double &a, double &b,
+                                           double &e, double &f) {
     constexpr int kU = 8;
-    int64_t r = r0;
-    for (; r + (kU - 1) * kAssembleThreads < r1; r += kU * kAssembleThreads) {
+    const int64_t e0 = g.n[0], e1 = e0 + g.n[1], e2 = e1 + g.n[2], e3 = e2 + g.n[3];
+    for (int64_t base = tid; base < e3; base += (int64_t)kU * kAssembleThreads) {
         double x[kU], y[kU];
 #pragma unroll
         for (int j = 0; j < kU; ++j) {
-            x[j] = __ldcg(lp0 + r + j * kAssembleThreads);
-            y[j] = __ldcg(lq + r + j * kAssembleThreads);
+            const int64_t i = base + (int64_t)j * kAssembleThreads;
+            x[j] = y[j] = 0.0;
+            if (i < e3) {
+                const bool r0 = i < e0, r1 = i < e1, r2 = i < e2;
+                const int64_t off = r0 ? g.o[0] + i
+                                       : (r1 ? g.o[1] + (i - e0)
+                                             : (r2 ? g.o[2] + (i - e1) : g.o[3] + (i - e2)));
+                const double *pl = r0 ? g.lp[0] : (r1 ? g.lp[1] : (r2 ? g.lp[2] : g.lp[3]));
+                const double *pq = r0 ? g.lq[0] : (r1 ? g.lq[1] : (r2 ? g.lq[2] : g.lq[3]));
+                x[j] = __ldcg(pl + off);
+                y[j] = __ldcg(pq + off);
+            }
         }
 #pragma unroll
         for (int j = 0; j < kU; ++j) {
-            a += x[j];
-            b += y[j];
-        }
-    }
-    double x[kU], y[kU];
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-        const int64_t rr = r + j * kAssembleThreads;
-        x[j] = rr < r1 ? __ldcg(lp0 + rr) : 0.0;
-        y[j] = rr < r1 ? __ldcg(lq + rr) : 0.0;
-    }
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-        if (r + j * kAssembleThreads < r1) {
-            a += x[j];
-            b += y[j];
+            const int64_t i = base + (int64_t)j * kAssembleThreads;
+            if (i < e0) {
+                a += x[j];
+                b += y[j];
+            } else if (i < e3) {
+                e += x[j];
+                f += y[j];
+            }
         }
     }
 }
@@ -87,8 +100,14 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
     pdl_launch_dependents();                         // the walk may be scheduled now
     const int c = chain_of(p.chain_seg0, p.n_chains, s);
+    // metadata in two rounds of loads: what depends on s (and c) only, then
+    // the root's and src's entries (indices clamped in range, checked below)
     const int32_t s0 = p.chain_seg0[c];
     const int32_t s1 = p.chain_seg0[c + 1];
+    const int32_t cs = p.seg_cut[s];
+    const int32_t src = p.seg_src[s];
+    const int64_t y0 = p.seg_row0[s];
+    const int64_t y1 = p.seg_row0[s + 1];
     if (s == s0) {                                   // a chain root
         if (tid == 0) {
             double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
@@ -101,27 +120,31 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     const int32_t T = p.T;
     int32_t bits = 0;
     if (s0 < 0 || s1 > p.n_seg || s1 <= s0 || s < s0 || s >= s1) bits |= PS_DEV_BAD_LAYOUT;
-    int32_t rc = 0, cs = 0, src = s0, csrc = T;
-    int64_t r0 = 0, y0 = 0, y1 = 0, q0 = 0, q1 = 0;
+    const int32_t s0l = bits ? s : s0;
+    const bool src_root = src == s0;
+    const bool src_ok = src_root || (src > s0 && src < s1 && src != s);
+    const int32_t srcl = (bits == 0 && src_ok) ? src : s;
+    const int32_t rc = p.seg_cut[s0l];
+    const int32_t rsrc = p.seg_src[s0l];
+    const int64_t r0 = p.seg_row0[s0l];
+    const int64_t r1 = p.seg_row0[s0l + 1];
+    const int32_t csrc_l = p.seg_cut[srcl];
+    const int64_t q0_l = p.seg_row0[srcl];
+    const int64_t q1_l = p.seg_row0[srcl + 1];
     if (bits == 0) {
-        rc = p.seg_cut[s0];
-        r0 = p.seg_row0[s0];
-        const int64_t r1 = p.seg_row0[s0 + 1];
-        if (p.seg_src[s0] != -1 || rc < 0 || rc > T || r0 < 0 || r1 > p.n_rows ||
+        if (rsrc != -1 || rc < 0 || rc > T || r0 < 0 || r1 > p.n_rows ||
             r1 - r0 != (int64_t)(T - rc))
             bits |= PS_DEV_BAD_LAYOUT;
-        cs = p.seg_cut[s];
-        src = p.seg_src[s];
-        y0 = p.seg_row0[s];
-        y1 = p.seg_row0[s + 1];
         if (cs < 0 || cs > T - 1 || y0 < 0 || y1 > p.n_rows || y1 - y0 != (int64_t)(T - cs))
             bits |= PS_DEV_BAD_LAYOUT;
-        if (src != s0 && (src <= s0 || src >= s1 || src == s)) bits |= PS_DEV_BAD_LAYOUT;
+        if (!src_ok) bits |= PS_DEV_BAD_LAYOUT;
     }
-    if (bits == 0 && src != s0) {
-        csrc = p.seg_cut[src];
-        q0 = p.seg_row0[src];
-        q1 = p.seg_row0[src + 1];
+    int32_t csrc = T;
+    int64_t q0 = 0, q1 = 0;
+    if (bits == 0 && !src_root) {
+        csrc = csrc_l;
+        q0 = q0_l;
+        q1 = q1_l;
         if (csrc < 0 || csrc > T - 1 || q0 < 0 || q1 > p.n_rows ||
             q1 - q0 != (int64_t)(T - csrc))
             bits |= PS_DEV_BAD_LAYOUT;
@@ -134,17 +157,19 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     pdl_wait_prerequisites();                        // per-row values are now visible
     if (bits == 0) {                                 // uniform across the block
         double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
-        range_sum(p.lp0, p.lq, y0 + tid, y1, a, b);
-        // the x suffix: positions cs+1..csrc of the current state (carried values
-        // up to the root's cut, root rows above it), then all rows of src
+        // y: the request's own rows.  x: positions cs+1..csrc of the current
+        // state (carried values up to the root's cut, root rows above it),
+        // then all rows of src
         const int32_t k1 = min(rc, csrc);               // last carried position
-        if (cs < k1) {
-            const int64_t base = (int64_t)c * T;
-            range_sum(p.root_lp0, p.root_lq, base + cs + tid, base + k1, e, f);
-        }
         const int32_t lo = max(cs, rc);                 // rows cover positions > rc
-        if (lo < csrc) range_sum(p.lp0, p.lq, r0 + (lo - rc) + tid, r0 + (csrc - rc), e, f);
-        range_sum(p.lp0, p.lq, q0 + tid, q1, e, f);
+        Ranges g;
+        g.lp[0] = p.lp0, g.lq[0] = p.lq, g.o[0] = y0, g.n[0] = y1 - y0;
+        g.lp[1] = p.root_lp0, g.lq[1] = p.root_lq, g.o[1] = (int64_t)c * T + cs;
+        g.n[1] = cs < k1 ? (int64_t)(k1 - cs) : 0;
+        g.lp[2] = p.lp0, g.lq[2] = p.lq, g.o[2] = r0 + (lo - rc);
+        g.n[2] = lo < csrc ? (int64_t)(csrc - lo) : 0;
+        g.lp[3] = p.lp0, g.lq[3] = p.lq, g.o[3] = q0, g.n[3] = q1 - q0;
+        ranges_sum(g, tid, a, b, e, f);
         a = warp_sum(a);
         b = warp_sum(b);
         e = warp_sum(e);

@@ -448,9 +448,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
     constexpr float kEntLimit = (float)(kVecPerLane * 16 / kEsz);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    // the next kernel (suffix sums) may be scheduled now; it waits for this
-    // grid to complete before it reads the per-row results
-    pdl_launch_dependents();
     const int64_t W = p.n_vwarps;
     const int64_t vw = (int64_t)blockIdx.x * kWarpsPerCta + wid;
     if (vw >= W) return;
@@ -668,6 +665,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             if (c + 1 < ce) row_start();
         }
     }
+    // the next kernel (suffix sums) may be launched once every CTA gets here;
+    // it still waits for this grid to complete before it reads the per-row
+    // results.  Triggering at the end rather than the start keeps its CTAs
+    // from waiting on the SMs through this kernel's tail, which measured
+    // slower on GB300.
+    pdl_launch_dependents();
 }
 
 template <int WARPS, int STAGES, int SB>
