@@ -361,19 +361,40 @@ __device__ __forceinline__ double neg_log1p_exp2(float a) {
 }
 
 // Entropy in nats from S1, Y1 (the sums without the token) and the token's
-// exponent t, all relative to the same reference; computed in float64 after
-// scaling by the larger of 2^t and S1.
-__device__ double entropy_nats(double s1, double y1, double t) {
+// exponent t, all relative to the same reference (the general form, for
+// shifts outside the range the fast form handles).
+__device__ double entropy_nats_wide(double s1, double y1, double t) {
     const bool tok = t != -INFINITY;
-    // no other finite logit: the token holds all the mass (its exponent is +inf
-    // then, since the reference never left -inf)
-    if (!(s1 > 0.0)) return tok ? 0.0 : __longlong_as_double(0x7ff8000000000000ll);
     const double m = fmax(tok ? t : -INFINITY, log2(s1));
-    if (m == -INFINITY) return __longlong_as_double(0x7ff8000000000000ll);
     const double et = tok ? exp2(t - m) : 0.0;
     const double zs = s1 * exp2(-m) + et;
     const double ms = y1 * exp2(-m) + (tok ? t * et : 0.0);
     return 0.6931471805599453 * (m + log2(zs) - ms / zs);
+}
+
+// The same with an integer shift m >= every exponent (m = ceil(max(t,
+// log2 S1))): Z = S1 2^-m + 2^(t-m) lies in (1/2, 2] and
+//     D = sum_j 2^(y_j - m) (m - y_j) = m Z - (Y1 2^-m + t 2^(t-m)) >= 0,
+//     H = ln 2 (log2 Z + D / Z).
+// D is formed in float64, since it is a difference of nearly equal terms when
+// one logit holds most of the mass; log2 Z and D / Z carry only float relative
+// error, so they are taken in float.  Few float64 operations: GB300's FP64
+// pipe is narrow, and this runs once per row.
+__device__ double entropy_nats(float s1, float y1, float t) {
+    const bool tok = t != -INFINITY;
+    // no other finite logit: the token holds all the mass (its exponent is +inf
+    // then, since the reference never left -inf)
+    if (!(s1 > 0.f)) return tok ? 0.0 : __longlong_as_double(0x7ff8000000000000ll);
+    const float m = ceilf(fmaxf(tok ? t : -INFINITY, log2f(s1)));
+    if (!(fabsf(m) < 1000.f))
+        return entropy_nats_wide((double)s1, (double)y1, tok ? (double)t : -INFINITY);
+    const double sc = __longlong_as_double((long long)(1023 - (int)m) << 52);   // 2^-m
+    const double et = tok ? (double)exp2f(t - m) : 0.0;
+    const double zs = fma((double)s1, sc, et);
+    const double ms = fma((double)y1, sc, tok ? (double)t * et : 0.0);
+    const double d = fma((double)m, zs, -ms);
+    const float zf = (float)zs;
+    return 0.6931471805599453 * ((double)log2f(zf) + (double)((float)d / zf));
 }
 
 template <int NP, bool ENT>
@@ -415,8 +436,7 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
             }
             if constexpr (ENT) {
                 // a token logit of -inf has no mass: t = -inf leaves it out
-                h = entropy_nats((double)a.s1, (double)a.y1,
-                                 lt == -INFINITY ? -INFINITY : (double)t);
+                h = entropy_nats(a.s1, a.y1, lt == -INFINITY ? -INFINITY : t);
             }
         }
     }
