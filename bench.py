@@ -250,6 +250,33 @@ def reference_arm(args, ws, rank):
     return 0
 
 
+def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
+    """Host-side tree construction (ps_build_bfs_tree, ps_predictive_allocation)
+    per call through the binding, for the bench's T and request budget.  The
+    predictive allocation runs on a complete binary candidate tree of depth 8
+    (511 nodes) with eq. (14) branch probabilities from seeded class
+    probabilities and the pages' default budget of 20."""
+    rng = np.random.default_rng(10086)
+    cuts = rng.integers(0, T, 8 * n_pf).astype(np.int32)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        ps.ps_build_bfs_tree(T, n_pf, None, cuts)
+    bfs_us = (time.perf_counter() - t0) / reps * 1e6
+    n = 511
+    acc = np.array([2 * v + 1 if 2 * v + 1 < n else -1 for v in range(n)], np.int32)
+    rej = np.array([2 * v + 2 if 2 * v + 2 < n else -1 for v in range(n)], np.int32)
+    pa, pr = rng.uniform(0, 0.6, n), rng.uniform(0, 0.4, n)
+    h = np.array([ps.ps_midpoint_branch_probability(a, r) for a, r in zip(pa, pr)])
+    cand = np.ones(n, np.uint8)
+    t0 = time.perf_counter()
+    for _ in range(reps // 10):
+        ps.ps_predictive_allocation(acc, rej, cand, h, 20)
+    dp_us = (time.perf_counter() - t0) / (reps // 10) * 1e6
+    return {"bfs_us": bfs_us, "bfs": f"T={T}, N_pf={n_pf}",
+            "dp_us": dp_us, "dp": "511-node candidate tree, budget 20",
+            "where": "host, per call through the binding"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -306,6 +333,16 @@ def main():
     mt_taus = [0.25, 0.5, 1.0]          # MultiTryMH candidate temperatures
     mt_lq = torch.empty((len(mt_taus), w.n_rows), dtype=torch.float64, device=dev)
     k1e, k1f = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cy_a, cy_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_ch, T = lay.n_chains, lay.T
+    cy_out = {k: torch.empty((n_ch, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
+    cy_prev = {k: torch.zeros((n_ch, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
+    cy_ll = torch.empty(n_ch, dtype=torch.float64, device=dev)
+    cy_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    carry_io = ps.make_carry_io(state_seg=d.t["state_seg"], row_lp0=d.t["lp0"], row_lq=d.t["lq"],
+                                prev_lp0=cy_prev["lp0"], prev_lq=cy_prev["lq"],
+                                next_lp0=cy_out["lp0"], next_lq=cy_out["lq"], loglik=cy_ll,
+                                status=cy_status)
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -332,6 +369,11 @@ def main():
             ps.ps_score_rows(d.batch, d.t["lp0"], d.t["lq"], d.t["status"], d.workspace,
                              stream, entropy=ent_rows)
         k1d.record(stream)
+        # the round carry-over (reached state's per-position values) after a step
+        cy_a.record(stream)
+        for _ in range(args.steps):
+            ps.ps_carry_state(d.batch, carry_io, stream)
+        cy_b.record(stream)
         # and the multi-temperature variant (log q at all three temperatures)
         k1e.record(stream)
         for _ in range(args.steps):
@@ -347,6 +389,8 @@ def main():
     k1_avg = k1a.elapsed_time(k1b) / args.steps
     k1_ent_avg = k1c.elapsed_time(k1d) / args.steps
     k1_mt_avg = k1e.elapsed_time(k1f) / args.steps
+    carry_ms = cy_a.elapsed_time(cy_b) / args.steps
+    assert int(cy_status.item()) == 0, ps.dev_status_names(int(cy_status.item()))
     st = int(d.t["status"].item())
     assert st == 0, ps.dev_status_names(st)
     ms_per_step = total_ms / args.steps
@@ -383,6 +427,10 @@ def main():
                          "logits_GBps": logits_bytes / (k1_ent_avg / 1e3) / 1e9},
         "multi_temperature": {"taus": mt_taus, "kernel_ms": k1_mt_avg,
                               "logits_GBps": logits_bytes / (k1_mt_avg / 1e3) / 1e9},
+        "carry": {"kernel_ms": carry_ms,
+                  "GBps": n_ch * T * 32 / (carry_ms / 1e3) / 1e9,
+                  "bytes": "per position: 16 B read (row or previous value), 16 B written"},
+        "tree_construction": host_tree_timing(ps, T, int(w.info.get("n_requests", 16))),
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
