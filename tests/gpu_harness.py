@@ -88,8 +88,10 @@ def oracle_rows(w, block_rows: int = 8192, threads: int | None = None):
     return lp0, lq, ent
 
 
-def run_oracle(w, threads: int | None = None) -> dict:
-    lp0, lq, ent = oracle_rows(w, threads=threads)
+def run_oracle(w, threads: int | None = None, rows=None) -> dict:
+    """The oracle on the workload; `rows` = (lp0, lq, entropy) per row when the
+    caller already has the oracle's per-row values (e.g. of a row pool)."""
+    lp0, lq, ent = oracle_rows(w, threads=threads) if rows is None else rows
     sums = oracle.suffix_sums(w.layout, lp0, lq)
     r, la = oracle.log_accept(sums, w.alpha)
     wk = oracle.walk(w.layout, la, w.u, w.max_steps)
@@ -180,11 +182,11 @@ def check_walk(w, g: dict, o: dict) -> dict:
     return dict(walk_near_ties=near, k_delta_mean=float(np.mean(g["k_delta"])))
 
 
-def full_parity(w, threads: int | None = None) -> dict:
+def full_parity(w, threads: int | None = None, rows=None) -> dict:
     g = run_gpu(w)
     assert g["status"] == 0, ps.dev_status_names(g["status"])
     assert g["wstatus"] == 0, ps.dev_status_names(g["wstatus"])
-    o = run_oracle(w, threads=threads)
+    o = run_oracle(w, threads=threads, rows=rows)
     stats = {}
     stats.update(check_rows(g, o))
     stats.update(check_log_accept(w, g, o))

@@ -15,6 +15,7 @@ from synth import make_workload
 from synth.trees import assemble_layout, bfs_tree
 from synth.workload import SWEEP5, Workload, draw_tokens, gen_logits, make_pool, workload_config5
 from tests import gpu_harness as H
+from tests.helpers import bf16_bits
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -59,16 +60,34 @@ def test_config4_full():
     assert 0.67 <= s["eps_certain"] <= 0.95
 
 
-def test_config5_sweep_points():
-    # a pool of distinct rows (> L2) read through a shuffled row index; the
-    # oracle scores each pool row once per token (tests/gpu_harness.py)
+@pytest.fixture(scope="module")
+def sweep_pool():
+    """The row pool of configuration 5 and the oracle's per-row values of every
+    pool row at each sweep temperature (tokens are drawn per (row, tau), so a
+    scored row's values depend only on its pool row and tau)."""
     taus = [1.0 / a for a in SWEEP5["alpha"]]
     pool, ptok = make_pool(8192, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus,
                            seed=10091, device=DEV)
-    for n_pf, T, alpha in [(4, 512, 2.0), (16, 1024, 8.0), (32, 2048, 4.0), (8, 2048, 2.0)]:
-        w = workload_config5(pool, ptok, n_pf, T, alpha, n_chains=256 if n_pf <= 16 else 64)
-        s = H.full_parity(w)
-        _report(f"config5 Npf={n_pf} T={T} a={alpha}", s)
+    lg = bf16_bits(pool)
+    vals = {}
+    for t in taus:
+        vals[float(t)] = oracle.row_logprobs(lg, "bf16", SWEEP5["V"], ptok[float(t)].cpu().numpy(),
+                                             t, entropy=True)
+    return pool, ptok, vals
+
+
+@pytest.mark.parametrize("T", SWEEP5["T"])
+@pytest.mark.parametrize("n_pf", SWEEP5["n_pf"])
+@pytest.mark.parametrize("alpha", SWEEP5["alpha"])
+def test_config5_sweep_point(sweep_pool, n_pf, T, alpha):
+    # 256 independent chains; rows read through a shuffled row index into a pool
+    # of distinct rows (> L2); every scored row is compared
+    pool, ptok, vals = sweep_pool
+    w = workload_config5(pool, ptok, n_pf, T, alpha, n_chains=256)
+    ri = w.row_index.cpu().numpy()
+    lp0, lq, ent = vals[float(w.tau)]
+    s = H.full_parity(w, rows=(lp0[ri], lq[ri], ent[ri]))
+    _report(f"config5 Npf={n_pf} T={T} a={alpha}", s)
 
 
 # ---- shapes, temperatures, edge cases ---------------------------------------
