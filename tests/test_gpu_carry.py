@@ -58,7 +58,7 @@ def test_carry_matches_oracle(cfg, kw):
                                atol=1e-7)
 
 
-def _round1(T, V, seed):
+def _first_round(T, V, seed):
     rng = np.random.default_rng(seed)
     tree = bfs_tree(rng, T, 8)
     tree.finalize_root_cut(0)                  # the root has rows for every position
@@ -66,19 +66,19 @@ def _round1(T, V, seed):
     x = gen_logits("boosted", dict(sigma=3.0, margin_mean=4.0), lay.n_rows, V, "bf16",
                    seed=seed + 1, device=DEV)
     tok = draw_tokens(x, 0.25, seed=seed + 2)
-    return Workload(name="round1", layout=lay, V=V, dtype="bf16", alpha=4.0, tau=0.25,
+    return Workload(name="first MH round", layout=lay, V=V, dtype="bf16", alpha=4.0, tau=0.25,
                     logits=x, tokens=tok, u=1.0 - rng.random(lay.n_seg), max_steps=100)
 
 
 def test_second_round_with_a_carried_current_state():
     T, V = 384, 151936
     for seed in (11, 12, 13):
-        w1 = _round1(T, V, seed)
+        w1 = _first_round(T, V, seed)
         d1 = _device(w1, entropy=False)
         carried = d1.carry()
         torch.cuda.synchronize()
         assert int(carried["status"].item()) == 0
-        # round 2: a fresh subtree rooted at the reached state
+        # the second MH round: a fresh subtree rooted at the reached state
         rng = np.random.default_rng(seed + 100)
         tree2 = bfs_tree(rng, T, 6)
         u2 = 1.0 - rng.random(len(tree2.seg_cut))

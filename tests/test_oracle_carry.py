@@ -63,7 +63,7 @@ def test_loglik_and_confidence_closed_form():
 
 
 def test_carried_root_gives_the_same_sums_as_scored_root_rows():
-    # two rounds: round 2's current state is round 1's reached state, given
+    # two MH rounds: the second round's current state is the first round's reached state, given
     # once as scored rows and once as carried per-position values
     rng = np.random.default_rng(3)
     T, V = 24, 60
@@ -76,13 +76,13 @@ def test_carried_root_gives_the_same_sums_as_scored_root_rows():
         _, la1 = oracle.log_accept(sums1, 4.0)
         u1 = 1.0 - rng.random(lay1.n_seg)
         wk = oracle.walk(lay1, la1, u1, 100)
-        # round 1's root covers positions rc+1..T; its prefix is carried from
+        # the first round's root covers positions rc+1..T; its prefix is carried from
         # an earlier round (arbitrary values here)
         rc1 = int(lay1.seg_cut[0])
         prev = {"lp0": rng.normal(size=(1, T)), "lq": rng.normal(size=(1, T))}
         carried = oracle.carry_state(lay1, wk["state_seg"], {"lp0": lp0_1, "lq": lq_1}, prev)
 
-        # round 2 tree, with the root's positions carried (root cut = T: no rows)
+        # the second round's tree, with the root's positions carried (root cut = T: no rows)
         tree2 = bfs_tree(rng, T, 4)
         tree2.finalize_root_cut(T)
         lay2c = assemble_layout([tree2])
@@ -93,7 +93,7 @@ def test_carried_root_gives_the_same_sums_as_scored_root_rows():
         sc = oracle.suffix_sums(lay2c, lp0_2, lq_2, root_lp0=carried["lp0"],
                                root_lq=carried["lq"])
 
-        # the same round 2 with the root given as rows: rows for positions
+        # the same second round with the root given as rows: rows for positions
         # 1..T whose values are the carried ones
         tree2.finalize_root_cut(0)
         lay2r = assemble_layout([tree2])
