@@ -85,6 +85,8 @@ typedef enum { PS_BF16 = 0, PS_F32 = 1 } ps_dtype;
  *              ld * element size >= V * element size rounded up to 16.
  *              Elements V..ld-1 of a row are ignored.  -inf is a valid logit
  *              (a masked token); NaN and +inf are reported as PS_DEV_NONFINITE.
+ *              A row holds at most 2^30 bytes (V <= 2^29 for bf16, 2^28 for
+ *              float32); larger V returns PS_ERR_INVALID_ARG.
  * row_index    [n_rows] int64 or NULL: scored row r reads logits row
  *              row_index[r]; NULL means row r reads logits row r (then
  *              n_logit_rows >= n_rows).

@@ -88,6 +88,7 @@ ps_status check_batch_host(const ps_subtree_batch *b, bool need_data = true) {
     if (esz == 0) return PS_ERR_UNSUPPORTED;
     if (!(b->tau > 0.0) || !isfinite(b->tau) || !isfinite(b->alpha)) return PS_ERR_INVALID_ARG;
     const int64_t row_bytes = ((int64_t)b->V * esz + 15) / 16 * 16;
+    if (row_bytes > (int64_t(1) << 30)) return PS_ERR_INVALID_ARG;   // chunk offsets are 32-bit
     if (b->ld < b->V || (b->ld * esz) % 16 != 0 || b->ld * esz < row_bytes)
         return PS_ERR_INVALID_ARG;
     if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;

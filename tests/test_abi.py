@@ -199,3 +199,27 @@ def test_wait_selftest_host_checks_need_no_gpu():
     assert ps.ps_selftest_wait_timeout(3_000_000_000, st, stream=0, check=False) == 1
     # a host pointer is not device memory
     assert ps.ps_selftest_wait_timeout(1_000_000, st, stream=0, check=False) == 1
+
+
+def test_row_size_limit_needs_no_gpu():
+    import torch
+    lay = assemble_layout([example5_tree(8, 5, 2)])
+    b, _ = _host(lay)
+    logits = torch.zeros(lay.n_rows, 64, dtype=torch.bfloat16)
+    toks = torch.zeros(lay.n_rows, dtype=torch.int32)
+    b.logits, b.tokens = logits.data_ptr(), toks.data_ptr()
+    lp0 = torch.zeros(lay.n_rows, dtype=torch.float64)
+    lq = torch.zeros(lay.n_rows, dtype=torch.float64)
+    st = torch.zeros(1, dtype=torch.int32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+
+    def call():
+        return ps.ps_score_rows(b, lp0, lq, st, ws, stream=0, check=False)
+
+    assert call() == 7                       # header accepted; stops at the workspace
+    b.V = b.ld = 1 << 29                     # bf16 rows of exactly 2^30 bytes: allowed
+    assert call() == 7
+    b.V = b.ld = (1 << 29) + 8               # above 2^30 bytes
+    assert call() == 1
+    b.dtype, b.V, b.ld = 1, (1 << 28) + 4, (1 << 28) + 4
+    assert call() == 1
