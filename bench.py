@@ -170,23 +170,39 @@ def build_workload(config: int, dev, rank: int, n_pf=None):
 
 
 def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
-    """The oracle, as it stands, on a bounded sample of the same batch."""
+    """The oracle, as it stands, on the same batch: per-row log-probabilities
+    (the step computes no entropy, so neither does this), the suffix sums over
+    explicit states, log A and the walk, on all host cores; and the per-row
+    part on one core over a sample of rows, extrapolated to the batch."""
     import oracle
     from tests.gpu_harness import oracle_rows   # block-wise host copies for the oracle
     threads = oracle.default_threads()
     lay = w.layout
-    # the whole batch: per-row log-probabilities (and entropy), the suffix
-    # sums over explicit states, log A and the walk
+    units = lay.suffix_tokens()
     t0 = time.time()
-    lp0, lq, _ent = oracle_rows(w, threads=threads)
+    lp0, lq, _ent = oracle_rows(w, threads=threads, entropy=False)
+    t1 = time.time()
     sums = oracle.suffix_sums(lay, lp0, lq)
     _, la = oracle.log_accept(sums, w.alpha)
     oracle.walk(lay, la, w.u, w.max_steps)
-    dt = time.time() - t0
-    units = lay.suffix_tokens()
+    t2 = time.time()
+    dt = t2 - t0
+    # one core: time growing row samples until one takes over max_seconds / 6
+    n1, tr1 = 64, 0.0
+    while True:
+        s0 = time.time()
+        oracle_rows(w, threads=1, entropy=False, n_rows=n1)
+        tr1 = time.time() - s0
+        if tr1 > max_seconds / 6 or n1 >= w.n_rows:
+            break
+        n1 = min(w.n_rows, n1 * 4)
+    one_core_s = tr1 * w.n_rows / n1 + (t2 - t1)
     return {"value": units / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"the whole batch ({w.n_rows} rows, {units} suffix tokens), "
-                      f"{dt:.1f} s wall on {threads} threads"}
+                      f"{dt:.1f} s wall on {threads} threads",
+            "one_core": {"value": units / one_core_s, "unit": UNIT, "cores": 1,
+                         "sample": f"per-row part timed on {n1} rows ({tr1:.1f} s) and "
+                                   f"scaled to {w.n_rows}; sums and walk as measured"}}
 
 
 def reference_arm(args, ws, rank):
