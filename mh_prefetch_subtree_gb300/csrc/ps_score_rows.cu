@@ -73,12 +73,17 @@ template <>
 struct Elem<PS_BF16> {
     static constexpr int kSize = 2;
     static constexpr uint32_t kNegInfWord = 0xff80ff80u;
+    static constexpr uint32_t kFloorWord = 0xf14af14au;   // two bf16 -1.0009e30
+    static constexpr uint16_t kFloorElem = 0xf14au;
 };
 template <>
 struct Elem<PS_F32> {
     static constexpr int kSize = 4;
     static constexpr uint32_t kNegInfWord = 0xff800000u;
+    static constexpr uint32_t kFloorWord = 0xf149f2cau;   // -1.0e30f
 };
+// Values at or below this are taken as absent (-inf) when the maximum is sought.
+constexpr float kAbsentBelow = -9.0e29f;
 
 __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -155,7 +160,10 @@ __device__ __forceinline__ float hsum4(const float2 (&a)[4]) {
 }
 
 // Sums of one lane's VPL vectors relative to reference R: c1, ct[0..NS-1], cy.
-template <int DT, int NP, bool ENT, int VPL>
+// CLAMP (entropy only) raises -inf inputs to a large negative finite value
+// first, so that 2^y y is 0 rather than NaN there; without it the caller must
+// see to it that no -inf is in q (a NaN sum sends the chunk down the slow path).
+template <int DT, int NP, bool ENT, int VPL, bool CLAMP = ENT>
 __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g, float &c1,
                                          float (&ct)[3], float &cy) {
     const float2 L2 = make_float2(kLog2e, kLog2e);
@@ -174,7 +182,7 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
         if constexpr (DT == PS_BF16) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if constexpr (ENT) w[j] = max_nan_bf16x2(w[j], kFloorBf16x2);
+                if constexpr (ENT && CLAMP) w[j] = max_nan_bf16x2(w[j], kFloorBf16x2);
                 const float2 v = make_float2(__uint_as_float(w[j] << 16),
                                              __uint_as_float(w[j] & 0xffff0000u));
                 step2<NP, ENT>(v, L2, nR2, G2, a1[j], at[j], ay[j]);
@@ -182,7 +190,7 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
         } else {
             float f[4] = {__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
                           __uint_as_float(w[3])};
-            if constexpr (ENT) {
+            if constexpr (ENT && CLAMP) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) f[j] = max_nan_f32(f[j], kFloorF32);
             }
@@ -233,8 +241,9 @@ __device__ __forceinline__ Acc rebase(Acc a, float Rn, float g) {
     return a;
 }
 
-// Load one lane's VPL vectors of a stage; vectors past the chunk read as -inf.
-template <int DT, int VPL>
+// Load one lane's VPL vectors of a stage; vectors past the chunk read as -inf
+// (or, with FLOOR, as the large negative finite floor).
+template <int DT, int VPL, bool FLOOR = false>
 __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
                                           uint4 (&q)[VPL]) {
     if (nvec == VPL * 32) {                    // a full chunk: no predication
@@ -242,7 +251,7 @@ __device__ __forceinline__ void load_vecs(const uint4 *v4, int nvec, int lane,
         for (int i = 0; i < VPL; ++i) q[i] = v4[lane + 32 * i];
         return;
     }
-    const uint32_t ni = Elem<DT>::kNegInfWord;
+    const uint32_t ni = FLOOR ? Elem<DT>::kFloorWord : Elem<DT>::kNegInfWord;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int idx = lane + 32 * i;
@@ -284,13 +293,18 @@ __device__ __noinline__ Acc slow_chunk(const uint4 *v4, int nvec, int lane, floa
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if constexpr (DT == PS_BF16) {
-                const float lo = __uint_as_float(w[j] << 16);
-                const float hi = __uint_as_float(w[j] & 0xffff0000u);
+                float lo = __uint_as_float(w[j] << 16);
+                float hi = __uint_as_float(w[j] & 0xffff0000u);
                 nan_seen |= (lo != lo) | (hi != hi);
+                if constexpr (ENT) {          // patched entries hold the floor
+                    lo = lo > kAbsentBelow ? lo : -INFINITY;
+                    hi = hi > kAbsentBelow ? hi : -INFINITY;
+                }
                 m = fmaxf(m, fmaxf(lo, hi));
             } else {
-                const float v = __uint_as_float(w[j]);
+                float v = __uint_as_float(w[j]);
                 nan_seen |= (v != v);
+                if constexpr (ENT) v = v > kAbsentBelow ? v : -INFINITY;
                 m = fmaxf(m, v);
             }
         }
@@ -586,20 +600,21 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
                     if constexpr (DT == PS_BF16) {
                         uint16_t *h = reinterpret_cast<uint16_t *>(buf) + o;
                         ltok = __uint_as_float((uint32_t)*h << 16);
-                        *h = 0xff80u;
+                        *h = ENT ? Elem<PS_BF16>::kFloorElem : 0xff80u;
                     } else {
                         float *f = reinterpret_cast<float *>(buf) + o;
                         ltok = *f;
-                        *f = -INFINITY;
+                        *f = ENT ? kFloorF32 : -INFINITY;
                     }
                 }
             }
             if (k == cpr - 1) {
                 for (int64_t j = (int64_t)p.V - e0; j < nel; ++j) {
                     if constexpr (DT == PS_BF16)
-                        reinterpret_cast<uint16_t *>(buf)[j] = 0xff80u;
+                        reinterpret_cast<uint16_t *>(buf)[j] = ENT ? Elem<PS_BF16>::kFloorElem
+                                                                   : 0xff80u;
                     else
-                        reinterpret_cast<float *>(buf)[j] = -INFINITY;
+                        reinterpret_cast<float *>(buf)[j] = ENT ? kFloorF32 : -INFINITY;
                 }
             }
         }
@@ -608,11 +623,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
             const int nvec = (int)(bytes >> 4);
             uint4 q[kVecPerLane];
-            load_vecs<DT, kVecPerLane>(v4, nvec, lane, q);
+            load_vecs<DT, kVecPerLane, ENT>(v4, nvec, lane, q);
             float c1, ct[3], cy;
-            sum_vecs<DT, NP, ENT, kVecPerLane>(q, acc.R, g, c1, ct, cy);
+            // the entropy variant's fast path skips the -inf clamp: the row's
+            // patches hold the floor, and a -inf input makes 2^y y NaN, which
+            // sends the chunk to the slow path (clamped)
+            sum_vecs<DT, NP, ENT, kVecPerLane, false>(q, acc.R, g, c1, ct, cy);
             bool fast = chunk_peak<NP>(c1, ct) <= kLimit;
-            if constexpr (ENT) fast = __all_sync(0xffffffffu, fast && c1 <= kEntLimit);
+            if constexpr (ENT)
+                fast = __all_sync(0xffffffffu, fast && c1 <= kEntLimit && cy == cy);
             if (fast) {
                 add_chunk<NP, ENT>(acc, c1, ct, cy);
             } else {
