@@ -40,8 +40,8 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
 # ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
-NCU_TRAFFIC = {"source_sha1": "203297a49ca51f17eced5857e0b8ba24c63a33e0",
-               "bytes_per_launch": 4160451584 + 3761664, "config": 2}
+NCU_TRAFFIC = {"source_sha1": "3f88b3b665b7adc3a8967ddc0d2de58a51fdc22f",
+               "bytes_per_launch": 4160486144 + 3944448, "config": 2}
 
 
 def log(*a):
