@@ -40,7 +40,7 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
 # ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
-NCU_TRAFFIC = {"source_sha1": "3f88b3b665b7adc3a8967ddc0d2de58a51fdc22f",
+NCU_TRAFFIC = {"source_sha1": "06638f83f68d5a25e55ee18c432067114417f147",
                "bytes_per_launch": 4160486144 + 3944448, "config": 2}
 
 
@@ -86,10 +86,18 @@ def peaks():
 
 
 def kernel_source_sha1() -> str:
+    """Hash of the scoring kernel's code (its two source files with comments,
+    blank lines and trailing blanks removed): the ncu traffic below is
+    reported only while the code it was captured from is unchanged."""
+    import re
     h = hashlib.sha1()
     for name in ("ps_score_rows.cu", "ps_internal.cuh"):
-        with open(os.path.join(ROOT, "mh_prefetch_subtree_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mh_prefetch_subtree_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        lines = [ln.rstrip() for ln in src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()
 
 

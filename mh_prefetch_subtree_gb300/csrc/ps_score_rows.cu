@@ -15,7 +15,9 @@
 // token holds nearly all the mass (the sums are then tiny, never 1 + tiny).
 // No maximum is needed: R only has to keep the exponentials in range.  Each
 // lane starts with R = -inf; a chunk whose sums overflow (or are NaN) takes a
-// slow path that raises R to the chunk's maximum and rescales.  When 1/tau is
+// slow path that raises R to the chunk's maximum and rescales.  (The entropy
+// variant keeps one R per warp and raises it whenever a chunk holds a logit
+// above it, so that a dominant logit is added close to R.)  When 1/tau is
 // 1, 2, 4 or 8 the tau exponential is the first one squared, so each logit
 // costs one MUFU ex2; the same squaring chain serves up to four such
 // temperatures in one pass (multi-temperature scoring).
@@ -28,7 +30,9 @@
 // completion on an mbarrier, L2 evict-first since every byte is read once);
 // the warp consumes a stage, refills it, and moves on.  There is no
 // block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
-// row's token logit (after saving it) and any padding beyond V with -inf.
+// row's token logit (after saving it) and any padding beyond V with -inf (in
+// the entropy variant with -1e30, which adds nothing either but keeps
+// 2^y y finite on the clamp-free fast path).
 //
 // A row whose chunks all lie in one warp's range is finalised by that warp.
 // A row split across warps leaves one partial per warp in the workspace; the
