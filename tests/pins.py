@@ -229,3 +229,114 @@ def pin_dominant_token(row_logprobs, V=1000):
     lp0, lq = row_logprobs(x, "f32", V, np.array([5], np.int32), 0.25)
     np.testing.assert_allclose(lq[0], -math.log1p((V - 1) * math.exp(-120.0)), rtol=1e-10)
     np.testing.assert_allclose(lp0[0], -math.log1p((V - 1) * math.exp(-30.0)), rtol=1e-10)
+
+
+# ---- next rows: entropy, epsilon classes, carry-over, tree construction -----
+
+def pin_entropy_library(entropy, V=700):
+    """entropy(x float32 [n, V]) against torch.distributions.Categorical in
+    float64 (a library routine), on rows with a peaked id and masked (-inf)
+    entries: catches a dropped normaliser, a sign error or a wrong base."""
+    import torch
+    rng = np.random.default_rng(21)
+    x = rng.normal(scale=3.0, size=(24, V)).astype(np.float32)
+    x[:, 3] += 10.0
+    x[5, 100:] = -np.inf
+    want = torch.distributions.Categorical(logits=torch.from_numpy(x.astype(np.float64))).entropy()
+    np.testing.assert_allclose(entropy(x), want.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def pin_entropy_uniform(entropy, V=1024):
+    """Uniform rows have H = log V exactly (closed form)."""
+    x = np.full((3, V), 1.25, np.float32)
+    np.testing.assert_allclose(entropy(x), math.log(V), rtol=1e-12)
+
+
+def pin_eps_classes(eps_class):
+    """Constructed values on both sides of eps and 1 - eps (section 3.3):
+    A <= eps is certain reject (0), A >= 1 - eps certain accept (2)."""
+    A = np.array([1.0, 0.995, 0.99, 0.5, 0.0101, 0.0099, 0.001, 0.0, np.nan])
+    with np.errstate(divide="ignore"):
+        la = np.log(A)
+    assert list(eps_class(la, 0.01)) == [2, 2, 2, 1, 1, 0, 0, 0, -1]
+
+
+def pin_carry_example5(carry_state):
+    """Example 5's walk reaches y = x_{0:c1} + y: the carried state takes the
+    previous values up to the root's cut, root rows up to c1, then y's rows
+    (rows are named by their index, so any misplaced position shows)."""
+    T, c1, c2 = 16, 9, 4
+    lay = assemble_layout([example5_tree(T, c1, c2)])
+    rc = int(lay.seg_cut[0])
+    prev = np.full((1, T), -7.0)
+    vals = np.arange(lay.n_rows, dtype=np.float64) + 0.5
+    out = carry_state(lay, np.array([1]), {"lp0": vals}, {"lp0": prev})
+    want = np.empty(T)
+    for t in range(1, T + 1):
+        if t <= rc:
+            want[t - 1] = -7.0
+        elif t <= c1:
+            want[t - 1] = lay.seg_row0[0] + (t - rc - 1) + 0.5
+        else:
+            want[t - 1] = lay.seg_row0[1] + (t - c1 - 1) + 0.5
+    assert np.array_equal(out["lp0"][0], want)
+
+
+def pin_bfs_example2(bfs):
+    """The pages' Example 2 (golden fixture): the first expansion's cut is
+    feasible under the root, its acceptance child expands next, the rejection
+    child keeps the root's cut."""
+    g = json.load(open(os.path.join(GOLDEN, "example2_bfs.json")))
+    T, c1, c2 = 20, 11, 6
+    t = bfs(T, g["n_pf"], None, [c1, c2])
+    assert t["acc"][0] == 1 and t["acc"][1] == 3 and t["rej"][0] == 2
+    assert list(t["seg_cut"][1:]) == [c1, c2] and list(t["seg_src"][1:]) == [0, 1]
+    assert t["req"][0] == 1 and t["req"][1] == 2 and t["node_cut"][0] == T
+
+
+def pin_bfs_condition1(bfs, trials=300):
+    """Condition 1 on random BFS trees: every scored request's cut is <= its
+    node's cut and its from-state's cut; deferred requests are the infeasible
+    ones; rejection children keep their parent's cut."""
+    rng = np.random.default_rng(1)
+    for _ in range(trials):
+        T = int(rng.integers(1, 50))
+        cuts = rng.integers(0, T, 200)
+        t = bfs(T, int(rng.integers(0, 15)), None if rng.random() < .5 else 4, cuts)
+        for v, r in enumerate(t["req"]):
+            if r >= 0:
+                assert t["seg_cut"][r] <= t["node_cut"][v]
+                src = t["seg_src"][r]
+                assert t["seg_cut"][r] <= (T if src == 0 else t["seg_cut"][src])
+            elif r == -2:
+                assert t["deferred"][v] > t["node_cut"][v]
+        for v in range(len(t["acc"])):
+            if t["rej"][v] >= 0:
+                assert t["node_cut"][t["rej"][v]] == t["node_cut"][v]
+
+
+def pin_dp_brute_force(allocation_dp, allocation_brute, reaching_weights, trials=40):
+    """eq. (19) against exhaustive search over ancestor-closed selections
+    (Proposition 2), and Lemma 1: the value is the selection's reaching weight."""
+    rng = np.random.default_rng(2)
+    for _ in range(trials):
+        acc, rej = [-1], [-1]
+        frontier = [(0, 0)]
+        while frontier:
+            v, d = frontier.pop()
+            if d < 3 and rng.random() < 0.85:
+                a, b = len(acc), len(acc) + 1
+                acc += [-1, -1]
+                rej += [-1, -1]
+                acc[v], rej[v] = a, b
+                frontier += [(a, d + 1), (b, d + 1)]
+        n = len(acc)
+        acc, rej = np.array(acc), np.array(rej)
+        cand = rng.random(n) < 0.8
+        cand[0] = True
+        h = rng.uniform(0.02, 0.98, n)
+        for budget in range(0, 6):
+            v, sel = allocation_dp(acc, rej, cand, h, budget)
+            assert abs(v - allocation_brute(acc, rej, cand, h, budget)) <= 1e-12
+            R = reaching_weights(acc, rej, h)
+            assert sel.sum() <= budget and abs(R[sel].sum() - v) <= 1e-12
