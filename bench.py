@@ -304,7 +304,7 @@ def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="libps", choices=["libps", "reference"])
     ap.add_argument("--config", type=int, default=2)
