@@ -459,6 +459,8 @@ def main():
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
                                      "walk_kernel": 1},
+        # what the suffix sums, log A and the walk add to a step after scoring
+        "after_scoring_us": (ms_per_step - k1_avg) * 1e3,
         "clocks": clocks.summary(),
     }
     if e2e is not None:
