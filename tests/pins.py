@@ -286,7 +286,8 @@ def pin_bfs_example2(bfs):
     """The pages' Example 2 (golden fixture): the first expansion's cut is
     feasible under the root, its acceptance child expands next, the rejection
     child keeps the root's cut."""
-    g = json.load(open(os.path.join(GOLDEN, "example2_bfs.json")))
+    with open(os.path.join(GOLDEN, "example2_bfs.json")) as fh:
+        g = json.load(fh)
     T, c1, c2 = 20, 11, 6
     t = bfs(T, g["n_pf"], None, [c1, c2])
     assert t["acc"][0] == 1 and t["acc"][1] == 3 and t["rej"][0] == 2

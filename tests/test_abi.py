@@ -22,7 +22,8 @@ def built():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "ps.h")).read()
+    with open(os.path.join(ROOT, "include", "ps.h")) as fh:
+        src = fh.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(ps_[a-z_]+)\s*\(", src)))
 

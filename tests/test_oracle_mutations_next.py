@@ -31,7 +31,7 @@ def _entropy_parts(x):
     js = x.argmax(axis=1)
     i = np.arange(x.shape[0])
     e[i, js] = 0.0
-    ed = np.where(e > 0, e * d, 0.0)
+    ed = e * np.where(e > 0, d, 0.0)              # -inf entries have e = 0
     return e.sum(1), ed.sum(1)
 
 

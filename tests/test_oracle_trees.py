@@ -13,7 +13,8 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 def test_bfs_example2():
-    g = json.load(open(os.path.join(GOLDEN, "example2_bfs.json")))
+    with open(os.path.join(GOLDEN, "example2_bfs.json")) as fh:
+        g = json.load(fh)
     T, c1, c2 = 20, 11, 6
     t = OT.bfs(T, g["n_pf"], None, [c1, c2])
     assert t["acc"][0] == 1 and t["acc"][1] == 3 and t["rej"][0] == 2

@@ -25,7 +25,8 @@ class _Scripted:
 
 
 def test_example2_bfs_order():
-    g = json.load(open(os.path.join(GOLDEN, "example2_bfs.json")))
+    with open(os.path.join(GOLDEN, "example2_bfs.json")) as fh:
+        g = json.load(fh)
     T, c1, c2 = 20, 11, 6
     t = bfs_tree(_Scripted([c1, c2]), T, g["n_pf"])
     assert t.n_requests == 2
