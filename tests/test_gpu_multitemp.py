@@ -158,3 +158,26 @@ def test_multi_rejects_unsupported_temperatures():
         lq = torch.empty(len(taus), n, dtype=torch.float64, device=DEV)
         assert ps.ps_score_rows_multi(d.batch, taus, lp0, lq, st, d.workspace,
                                       check=False) == ps.PS_ERR_UNSUPPORTED
+
+
+def test_multi_temperature_through_a_row_index():
+    # rows read through a shuffled row index into a pool (the sweep's layout):
+    # every temperature against the oracle on the pool row each scored row reads
+    V = 151936
+    rng = np.random.default_rng(31)
+    n_pool = 600
+    pool = gen_logits("boosted", dict(sigma=3.0, margin_mean=4.0), n_pool, V, "bf16", seed=32,
+                      device=DEV)
+    lay = assemble_layout([bfs_tree(rng, 40, 6) for _ in range(8)])
+    ri = torch.from_numpy(rng.integers(0, n_pool, lay.n_rows).astype(np.int64)).to(DEV)
+    tok = torch.from_numpy(rng.integers(0, V, lay.n_rows).astype(np.int32)).to(DEV)
+    d = ps.DeviceSubtree.create(layout=lay, u=1.0 - rng.random(lay.n_seg), logits=pool,
+                                tokens=tok, V=V, alpha=4.0, tau=0.25, max_steps=10,
+                                row_index=ri, entropy=True)
+    lp0, lq, ent, status = _run_multi(d, TABLE6_TAUS)
+    assert status == 0
+    lg = bf16_bits(pool)
+    for k, t in enumerate(TABLE6_TAUS):
+        o = oracle.row_logprobs(lg, "bf16", V, tok.cpu().numpy(), t,
+                                row_index=ri.cpu().numpy(), entropy=True)
+        _check((lp0, lq[k], ent), o, f"row_index tau={t}")
