@@ -177,6 +177,19 @@ def build_workload(config: int, dev, rank: int, n_pf=None):
     return make_workload(config, device=dev, **kw)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
     """The oracle, as it stands, on the same batch: per-row log-probabilities
     (the step computes no entropy, so neither does this), the suffix sums over
@@ -206,6 +219,7 @@ def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
         n1 = min(w.n_rows, n1 * 4)
     one_core_s = tr1 * w.n_rows / n1 + (t2 - t1)
     return {"value": units / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(), "nproc": os.cpu_count(),
             "sample": f"the whole batch ({w.n_rows} rows, {units} suffix tokens), "
                       f"{dt:.1f} s wall on {threads} threads",
             "one_core": {"value": units / one_core_s, "unit": UNIT, "cores": 1,
