@@ -288,6 +288,68 @@ def reference_arm(args, ws, rank):
     return 0
 
 
+def sweep(args) -> int:
+    """--sweep: the throughput sweep (256 independent chains x N_pf x T x alpha,
+    tau = 1/alpha, rows read through a shuffled row index into a pool of 8192
+    distinct rows, 2.5 GB > L2).  Prints one JSON line per point and one with
+    the aggregate; informative, not the bench line."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import mh_prefetch_subtree_gb300 as ps
+    from synth.workload import SWEEP5, make_pool, workload_config5
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    taus = [1.0 / a for a in SWEEP5["alpha"]]
+    pool, ptok = make_pool(8192, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus, seed=10091,
+                           device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    tot_tokens, tot_ms, tot_bytes, tot_k1 = 0, 0.0, 0.0, 0.0
+    for n_pf in SWEEP5["n_pf"]:
+        for T in SWEEP5["T"]:
+            for alpha in SWEEP5["alpha"]:
+                w = workload_config5(pool, ptok, n_pf, T, alpha, n_chains=256)
+                d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits,
+                                            tokens=w.tokens, V=w.V, alpha=w.alpha, tau=w.tau,
+                                            max_steps=w.max_steps, row_index=w.row_index)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup):
+                        d.score_rows(stream), d.assemble(stream), d.walk(stream)
+                    torch.cuda.synchronize()
+                    ev[0].record(stream)
+                    for _ in range(args.sweep_steps):
+                        d.score_rows(stream), d.assemble(stream), d.walk(stream)
+                    ev[1].record(stream)
+                    ev[2].record(stream)
+                    for _ in range(args.sweep_steps):
+                        d.score_rows(stream)
+                    ev[3].record(stream)
+                torch.cuda.synchronize()
+                st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
+                assert st == 0, ps.dev_status_names(st)
+                ms = ev[0].elapsed_time(ev[1]) / args.sweep_steps
+                k1 = ev[2].elapsed_time(ev[3]) / args.sweep_steps
+                units = w.layout.suffix_tokens()
+                nbytes = w.n_rows * w.V * 2
+                tot_tokens += units
+                tot_ms += ms
+                tot_bytes += nbytes
+                tot_k1 += k1
+                print(json.dumps({"sweep_point": {"n_pf": n_pf, "T": T, "alpha": alpha,
+                                                  "rows": w.n_rows, "suffix_tokens": units,
+                                                  "ms_per_step": ms, "tokens_per_s": units / ms * 1e3,
+                                                  "k1_ms": k1,
+                                                  "logits_GBps": nbytes / k1 / 1e6}}), flush=True)
+                del d, w
+    print(json.dumps({"sweep": {"points": len(SWEEP5["n_pf"]) * len(SWEEP5["T"]) *
+                                len(SWEEP5["alpha"]), "n_chains": 256,
+                                "tokens_per_s": tot_tokens / tot_ms * 1e3,
+                                "logits_GBps": tot_bytes / tot_k1 / 1e6,
+                                "note": "each point's step timed alone; totals over all points"}}),
+          flush=True)
+    return 0
+
+
 def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
     """Host-side tree construction (ps_build_bfs_tree, ps_predictive_allocation)
     per call through the binding, for the bench's T and request budget.  The
@@ -325,6 +387,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the 36-point throughput sweep instead (informative)")
+    ap.add_argument("--sweep-steps", type=int, default=5)
     ap.add_argument("--n-pf", type=int, default=None,
                     help="override the request budget (smaller batches for profiling)")
     args = ap.parse_args()
@@ -333,6 +398,8 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return reference_arm(args, ws, rank)
+    if args.sweep:
+        return sweep(args) if rank == 0 else 0
 
     import __graft_entry__
     __graft_entry__.build()
