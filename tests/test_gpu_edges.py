@@ -93,3 +93,52 @@ def test_many_small_chains_in_one_launch():
     trees += [bfs_tree(rng, T, int(rng.integers(0, 6))) for _ in range(1999)]
     w = _workload(trees, 512, dtype="f32", seed=65)
     H.full_parity(w)
+
+
+def test_bad_uniform_is_flagged_and_rejects():
+    # u outside (0, 1] is reported (PS_DEV_BAD_UNIFORM) and that decision rejects
+    rng = np.random.default_rng(66)
+    w = _workload([bfs_tree(rng, 16, 4) for _ in range(3)], 2048, seed=66)
+    lay = w.layout
+    s_bad = int(lay.req[int(lay.chain_node0[1])])      # the first decision of chain 1
+    u = w.u.copy()
+    u[s_bad] = 0.0
+    w.u = u
+    g = H.run_gpu(w)
+    assert g["wstatus"] & 0x80
+    root1 = int(lay.chain_node0[1])
+    assert g["path"][1 * (w.max_steps + 1) + 1] == int(lay.rej[root1])   # went right
+
+
+def test_request_whose_src_is_in_another_chain_is_flagged():
+    # a layout the host validator would reject, given to the device anyway:
+    # the request gets NaN and PS_DEV_BAD_LAYOUT, the others are unaffected
+    rng = np.random.default_rng(67)
+    w = _workload([bfs_tree(rng, 16, 4) for _ in range(2)], 2048, seed=67)
+    lay = w.layout
+    bad = int(lay.chain_seg0[1]) + 1                    # first request of chain 1
+    lay.seg_src = lay.seg_src.copy()
+    lay.seg_src[bad] = 1                                # a request of chain 0
+    g = H.run_gpu(w)
+    assert g["status"] & 0x10
+    assert np.isnan(g["log_accept"][bad])
+    ok = ~lay.is_root()
+    ok[bad] = False
+    assert np.isfinite(g["log_accept"][ok]).all()
+
+
+def test_carry_with_a_foreign_state_is_flagged():
+    import mh_prefetch_subtree_gb300 as ps
+    rng = np.random.default_rng(68)
+    w = _workload([bfs_tree(rng, 16, 4) for _ in range(2)], 2048, seed=68)
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens, V=w.V,
+                                alpha=w.alpha, tau=w.tau, max_steps=w.max_steps)
+    d.step()
+    torch.cuda.synchronize()
+    d.t["state_seg"][1] = 1                             # chain 1 "reached" chain 0's segment
+    T = w.layout.T
+    prev = {k: torch.zeros((2, T), dtype=torch.float64, device=DEV) for k in ("lp0", "lq")}
+    out = d.carry(prev)
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) & 0x10
+    assert torch.isnan(out["lp0"][1]).all() and torch.isfinite(out["lp0"][0]).all()
