@@ -78,6 +78,16 @@ typedef enum { PS_BF16 = 0, PS_F32 = 1 } ps_dtype;
 #define PS_NODE_DEFERRED (-2)     /* its request was deferred: the walk stops here */
 
 /*
+ * Batch hints.  PS_FLAG_MASKED_LOGITS: the logits may hold many -inf entries
+ * (a masked vocabulary).  Results are the same with or without it.  Without
+ * it the entropy variant's fast path assumes finite logits, and a chunk with a
+ * -inf input is summed again on its slow path (about 2x the time on a mostly
+ * masked row).  With it the fast path clamps -inf itself, which costs
+ * ordinary rows about 3%.
+ */
+#define PS_FLAG_MASKED_LOGITS 0x1
+
+/*
  * One subtree batch to score (section 3.2 step (2); eq. (6)).
  *
  * logits       [n_logit_rows][ld] row-major, dtype; base 16-byte aligned and
@@ -117,7 +127,7 @@ typedef struct {
     int32_t dtype;          /* ps_dtype */
     int32_t n_chains;
     int32_t n_seg;
-    int32_t reserved0;      /* must be 0 */
+    int32_t flags;          /* PS_FLAG_* hints; other bits must be 0 */
     int64_t n_rows;
     int64_t ld;
     int64_t n_logit_rows;

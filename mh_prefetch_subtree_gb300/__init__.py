@@ -28,6 +28,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libps.so")
 
 PS_OK = 0
+PS_FLAG_MASKED_LOGITS = 0x1
 PS_ERR_INVALID_ARG, PS_ERR_INFEASIBLE, PS_ERR_BAD_TREE, PS_ERR_UNSUPPORTED = 1, 2, 3, 4
 PS_ERR_CUDA, PS_ERR_TIMEOUT, PS_ERR_WORKSPACE = 5, 6, 7
 PS_BF16, PS_F32 = 0, 1
@@ -43,7 +44,7 @@ _vp = ctypes.c_void_p
 class PsSubtreeBatch(ctypes.Structure):
     _fields_ = [("V", ctypes.c_int32), ("T", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("n_chains", ctypes.c_int32), ("n_seg", ctypes.c_int32),
-                ("reserved0", ctypes.c_int32), ("n_rows", ctypes.c_int64),
+                ("flags", ctypes.c_int32), ("n_rows", ctypes.c_int64),
                 ("ld", ctypes.c_int64), ("n_logit_rows", ctypes.c_int64),
                 ("alpha", ctypes.c_double), ("tau", ctypes.c_double),
                 ("eps", ctypes.c_double), ("chain_seg0", _vp), ("seg_row0", _vp), ("seg_cut", _vp), ("seg_src", _vp),
@@ -376,7 +377,7 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
                seg_src, logits=None, tokens=None, row_index=None, n_rows: int | None = None,
                n_logit_rows: int | None = None, ld: int | None = None,
                dtype: int | None = None, eps: float = 0.01, root_lp0=None,
-               root_lq=None) -> PsSubtreeBatch:
+               root_lq=None, flags: int = 0) -> PsSubtreeBatch:
     """Fill a ps_subtree_batch from tensors (device for scoring, host for validation)."""
     _need(chain_seg0, torch.int32, "chain_seg0")
     _need(seg_row0, torch.int64, "seg_row0")
@@ -390,7 +391,7 @@ def make_batch(*, V: int, T: int, alpha: float, tau: float, chain_seg0, seg_row0
     b.V, b.T = int(V), int(T)
     b.n_chains = int(chain_seg0.shape[0]) - 1
     b.n_seg = int(seg_cut.shape[0])
-    b.reserved0 = 0
+    b.flags = int(flags)
     if n_rows is None:
         n_rows = int(tokens.shape[0]) if tokens is not None else 0
     b.n_rows = int(n_rows)
@@ -493,7 +494,7 @@ class DeviceSubtree:
                per_row: bool = True, sums: bool = True, path: bool = True,
                entropy: bool = False, eps: float | None = None,
                root_lp0: torch.Tensor | None = None,
-               root_lq: torch.Tensor | None = None) -> "DeviceSubtree":
+               root_lq: torch.Tensor | None = None, flags: int = 0) -> "DeviceSubtree":
         dev = logits.device
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
         t = dict(
@@ -527,7 +528,7 @@ class DeviceSubtree:
                            seg_row0=t["seg_row0"], seg_cut=t["seg_cut"], seg_src=t["seg_src"],
                            logits=logits, tokens=tokens, row_index=row_index, n_rows=n_rows,
                            eps=0.01 if eps is None else eps, root_lp0=root_lp0,
-                           root_lq=root_lq)
+                           root_lq=root_lq, flags=flags)
         ws_bytes = ps_score_workspace_bytes(batch)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         sout = make_score_out(log_accept=t["log_accept"], status=t["status"], lp0=t["lp0"],

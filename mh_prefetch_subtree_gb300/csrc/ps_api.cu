@@ -83,7 +83,7 @@ ps_status check_batch_host(const ps_subtree_batch *b, bool need_data = true) {
     if (!b) return PS_ERR_INVALID_ARG;
     if (b->V < 1 || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)
         return PS_ERR_INVALID_ARG;
-    if (b->reserved0 != 0) return PS_ERR_INVALID_ARG;
+    if (b->flags & ~PS_FLAG_MASKED_LOGITS) return PS_ERR_INVALID_ARG;
     const int esz = elem_size(b->dtype);
     if (esz == 0) return PS_ERR_UNSUPPORTED;
     if (!(b->tau > 0.0) || !isfinite(b->tau) || !isfinite(b->alpha)) return PS_ERR_INVALID_ARG;
@@ -157,6 +157,7 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
     p.n_rows = b->n_rows;
     p.V = b->V;
     p.dtype = b->dtype;
+    p.flags = b->flags;
     p.row_bytes = (int32_t)(((int64_t)b->V * esz + 15) / 16 * 16);
     p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
     p.n_chunks = b->n_rows * p.cpr;
@@ -501,6 +502,7 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
         p.n_rows = b->n_rows;
         p.V = b->V;
         p.dtype = b->dtype;
+        p.flags = b->flags;
         p.row_bytes = (int32_t)(((int64_t)b->V * esz + 15) / 16 * 16);
         p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
         p.n_chunks = b->n_rows * p.cpr;

@@ -42,6 +42,7 @@ struct RowsParams {
     int64_t n_rows;
     int32_t V;
     int32_t dtype;              // PS_BF16 / PS_F32
+    int32_t flags;              // PS_FLAG_* hints of the batch
     int32_t row_bytes;          // V * elem rounded up to 16
     int32_t cpr;                // chunks per row
     int64_t n_chunks;           // n_rows * cpr

@@ -463,8 +463,9 @@ __device__ void finalize_row(const RowsParams &p, int64_t r, Acc a, float lt, bo
     if constexpr (ENT) p.entropy[r] = h;
 }
 
-// WARPS warps per CTA, each with a ring of STAGES stages of SB bytes.
-template <int DT, int NP, bool ENT, int WARPS, int STAGES, int SB>
+// WARPS warps per CTA, each with a ring of STAGES stages of SB bytes.  CF
+// (entropy only): clamp -inf in the fast path too (PS_FLAG_MASKED_LOGITS).
+template <int DT, int NP, bool ENT, int WARPS, int STAGES, int SB, bool CF>
 __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kWarpsPerCta = WARPS;
@@ -629,10 +630,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
             uint4 q[kVecPerLane];
             load_vecs<DT, kVecPerLane, ENT>(v4, nvec, lane, q);
             float c1, ct[3], cy;
-            // the entropy variant's fast path skips the -inf clamp: the row's
-            // patches hold the floor, and a -inf input makes 2^y y NaN, which
-            // sends the chunk to the slow path (clamped)
-            sum_vecs<DT, NP, ENT, kVecPerLane, false>(q, acc.R, g, c1, ct, cy);
+            // the entropy variant's fast path skips the -inf clamp (unless the
+            // batch says its logits may be masked): the row's patches hold the
+            // floor, and a -inf input makes 2^y y NaN, which sends the chunk to
+            // the slow path (clamped)
+            sum_vecs<DT, NP, ENT, kVecPerLane, ENT && CF>(q, acc.R, g, c1, ct, cy);
             bool fast = chunk_peak<NP>(c1, ct) <= kLimit;
             if constexpr (ENT)
                 fast = __all_sync(0xffffffffu, fast && c1 <= kEntLimit && cy == cy);
@@ -721,9 +723,9 @@ constexpr size_t smem_bytes_for() {
     return (size_t)WARPS * STAGES * SB + (size_t)WARPS * STAGES * 8;
 }
 
-template <int DT, int NP, bool ENT>
+template <int DT, int NP, bool ENT, bool CF>
 cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    auto kern = score_rows_kernel<DT, NP, ENT, kWarpsPerCta, kStages, kStageBytes>;
+    auto kern = score_rows_kernel<DT, NP, ENT, kWarpsPerCta, kStages, kStageBytes, CF>;
     const size_t smem = smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -732,17 +734,24 @@ cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int DT, bool ENT>
+template <int DT, bool ENT, bool CF>
 cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
     switch (p.npow) {
-        case 1: return launch_t<DT, 1, ENT>(p, n_ctas, stream);
-        case 2: return launch_t<DT, 2, ENT>(p, n_ctas, stream);
-        case 4: return launch_t<DT, 4, ENT>(p, n_ctas, stream);
-        case 8: return launch_t<DT, 8, ENT>(p, n_ctas, stream);
-        case kAllPowers: return launch_t<DT, kAllPowers, ENT>(p, n_ctas, stream);
-        case kPowersTo4: return launch_t<DT, kPowersTo4, ENT>(p, n_ctas, stream);
-        default: return launch_t<DT, 0, ENT>(p, n_ctas, stream);
+        case 1: return launch_t<DT, 1, ENT, CF>(p, n_ctas, stream);
+        case 2: return launch_t<DT, 2, ENT, CF>(p, n_ctas, stream);
+        case 4: return launch_t<DT, 4, ENT, CF>(p, n_ctas, stream);
+        case 8: return launch_t<DT, 8, ENT, CF>(p, n_ctas, stream);
+        case kAllPowers: return launch_t<DT, kAllPowers, ENT, CF>(p, n_ctas, stream);
+        case kPowersTo4: return launch_t<DT, kPowersTo4, ENT, CF>(p, n_ctas, stream);
+        default: return launch_t<DT, 0, ENT, CF>(p, n_ctas, stream);
     }
+}
+
+template <int DT>
+cudaError_t launch_ent(const RowsParams &p, int n_ctas, cudaStream_t stream) {
+    if (p.entropy == nullptr) return launch_dt<DT, false, false>(p, n_ctas, stream);
+    if (p.flags & PS_FLAG_MASKED_LOGITS) return launch_dt<DT, true, true>(p, n_ctas, stream);
+    return launch_dt<DT, true, false>(p, n_ctas, stream);
 }
 
 }  // namespace
@@ -750,12 +759,8 @@ cudaError_t launch_dt(const RowsParams &p, int n_ctas, cudaStream_t stream) {
 size_t score_rows_smem_bytes() { return smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>(); }
 
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    const bool ent = p.entropy != nullptr;
-    if (p.dtype == PS_BF16)
-        return ent ? launch_dt<PS_BF16, true>(p, n_ctas, stream)
-                   : launch_dt<PS_BF16, false>(p, n_ctas, stream);
-    return ent ? launch_dt<PS_F32, true>(p, n_ctas, stream)
-               : launch_dt<PS_F32, false>(p, n_ctas, stream);
+    if (p.dtype == PS_BF16) return launch_ent<PS_BF16>(p, n_ctas, stream);
+    return launch_ent<PS_F32>(p, n_ctas, stream);
 }
 
 }  // namespace ps

@@ -224,3 +224,20 @@ def test_row_size_limit_needs_no_gpu():
     assert call() == 1
     b.dtype, b.V, b.ld = 1, (1 << 28) + 4, (1 << 28) + 4
     assert call() == 1
+
+
+def test_batch_flags_need_no_gpu():
+    import torch
+    lay = assemble_layout([example5_tree(8, 5, 2)])
+    b, _ = _host(lay)
+    logits = torch.zeros(lay.n_rows, 64, dtype=torch.bfloat16)
+    toks = torch.zeros(lay.n_rows, dtype=torch.int32)
+    b.logits, b.tokens = logits.data_ptr(), toks.data_ptr()
+    lp0 = torch.zeros(lay.n_rows, dtype=torch.float64)
+    lq = torch.zeros(lay.n_rows, dtype=torch.float64)
+    st = torch.zeros(1, dtype=torch.int32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    b.flags = ps.PS_FLAG_MASKED_LOGITS          # a known hint: passes to the workspace check
+    assert ps.ps_score_rows(b, lp0, lq, st, ws, stream=0, check=False) == 7
+    b.flags = 0x2                               # an unknown bit
+    assert ps.ps_score_rows(b, lp0, lq, st, ws, stream=0, check=False) == 1

@@ -206,6 +206,26 @@ def test_masked_vocabulary():
     _report("masked", H.full_parity(w))
 
 
+def test_masked_vocabulary_with_the_masked_hint():
+    # PS_FLAG_MASKED_LOGITS changes only how the entropy variant sums: results
+    # match the oracle as without it
+    w = _small(151936, "bf16", T=10, n_pf=4, n_chains=2, seed=15)
+    x = w.logits.clone()
+    x[:, 2000:] = float("-inf")
+    x[0, :] = float("-inf")
+    x[0, 7] = 1.0                                # one finite logit
+    w.logits = x
+    w.tokens = draw_tokens(x, w.tau, seed=16)
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
+                                entropy=True, eps=H.EPS, flags=ps.PS_FLAG_MASKED_LOGITS)
+    d.step()
+    torch.cuda.synchronize()
+    assert int(d.t["status"].item()) == 0
+    g = {k: d.t[k].cpu().numpy() for k in ("lp0", "lq", "entropy")}
+    _report("masked hint", H.check_rows(g, H.run_oracle(w)))
+
+
 def test_status_bits_and_nan_outputs():
     w = _small(4096, "bf16", T=8, n_pf=3, n_chains=1, seed=13)
     tok = w.tokens.clone()
