@@ -40,8 +40,8 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes per launch of the scoring kernel on the default workload, from one
 # ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
-NCU_TRAFFIC = {"source_sha1": "06638f83f68d5a25e55ee18c432067114417f147",
-               "bytes_per_launch": 4160486144 + 3944448, "config": 2}
+NCU_TRAFFIC = {"source_sha1": "726286a81d5ed43f45d983e626b4d6049846d235",
+               "bytes_per_launch": 4160389120 + 3825920, "config": 2}
 
 
 def log(*a):
