@@ -181,3 +181,17 @@ def test_multi_temperature_through_a_row_index():
         o = oracle.row_logprobs(lg, "bf16", V, tok.cpu().numpy(), t,
                                 row_index=ri.cpu().numpy(), entropy=True)
         _check((lp0, lq[k], ent), o, f"row_index tau={t}")
+
+
+@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (4097, "f32")])
+def test_multi_temperature_on_masked_rows_with_and_without_the_hint(V, dtype):
+    d, x, tok = _rows(V, dtype, TABLE6_TAUS, T=10, n_pf=4, n_chains=2, seed=41,
+                      ld=4100 if dtype == "f32" else None)
+    x[:, 700:V] = float("-inf")                       # a masked vocabulary
+    tok.copy_(tok % 700)
+    for flags in (0, ps.PS_FLAG_MASKED_LOGITS):
+        d.batch.flags = flags
+        lp0, lq, ent, status = _run_multi(d, TABLE6_TAUS)
+        assert status == 0
+        for k, t in enumerate(TABLE6_TAUS):
+            _check((lp0, lq[k], ent), _oracle(x, dtype, V, tok, t), f"flags={flags} tau={t}")
