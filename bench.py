@@ -350,6 +350,75 @@ def sweep(args) -> int:
     return 0
 
 
+def steady_state_leg(ps, w, d, dev, stream, steps: int, warmup: int) -> dict:
+    """The same round as the timed step, with the current state's per-position
+    values carried from the previous round (the pages keep them; ps_carry_state
+    produces them) instead of its rows scored again: the step scores only the
+    requests' rows (through a row index into the same logits), assembles with
+    the carried values, walks, and carries the reached state forward.
+    Informative; the bench line scores the root rows."""
+    import copy
+    from synth.trees import assemble_layout
+    lay = w.layout
+    T = lay.T
+    trees = [copy.deepcopy(t) for t in lay.trees]
+    for t in trees:
+        t.finalize_root_cut(T)                   # no root rows
+    lay2 = assemble_layout(trees)
+    keep, root_lp0, root_lq = [], [], []
+    lp0_h, lq_h = d.t["lp0"].cpu().numpy(), d.t["lq"].cpu().numpy()
+    for c in range(lay.n_chains):
+        s0, s1 = int(lay.chain_seg0[c]), int(lay.chain_seg0[c + 1])
+        r0, r1 = int(lay.seg_row0[s0]), int(lay.seg_row0[s0 + 1])
+        rc = int(lay.seg_cut[s0])
+        vals0, valsq = np.zeros(T), np.zeros(T)   # positions <= rc: earlier rounds' values
+        vals0[rc:], valsq[rc:] = lp0_h[r0:r1], lq_h[r0:r1]
+        root_lp0.append(vals0)
+        root_lq.append(valsq)
+        keep.extend(range(int(lay.seg_row0[s0 + 1]), int(lay.seg_row0[s1])))
+    assert len(keep) == lay2.n_rows
+    ri = torch.tensor(keep, dtype=torch.int64, device=dev)
+    rl0 = torch.tensor(np.stack(root_lp0), dtype=torch.float64, device=dev)
+    rlq = torch.tensor(np.stack(root_lq), dtype=torch.float64, device=dev)
+    d2 = ps.DeviceSubtree.create(layout=lay2, u=w.u, logits=w.logits, tokens=w.tokens[ri],
+                                 V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
+                                 row_index=ri, root_lp0=rl0, root_lq=rlq)
+    nxt = {k: torch.empty((lay.n_chains, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
+    cst = torch.zeros(1, dtype=torch.int32, device=dev)
+    io = ps.make_carry_io(state_seg=d2.t["state_seg"], row_lp0=d2.t["lp0"], row_lq=d2.t["lq"],
+                          prev_lp0=rl0, prev_lq=rlq, next_lp0=nxt["lp0"], next_lq=nxt["lq"],
+                          status=cst)
+
+    def one():
+        d2.score_rows(stream)
+        d2.assemble(stream)
+        d2.walk(stream)
+        ps.ps_carry_state(d2.batch, io, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    st = int(d2.t["status"].item()) | int(d2.t["wstatus"].item()) | int(cst.item())
+    assert st == 0, ps.dev_status_names(st)
+    # the same log A as the step that scored the root rows
+    req = ~lay.is_root()
+    dla = np.abs(d2.t["log_accept"].cpu().numpy()[req] - d.t["log_accept"].cpu().numpy()[req])
+    assert float(dla.max()) <= 1e-4, float(dla.max())
+    ms = a.elapsed_time(b) / steps
+    units = lay.suffix_tokens()
+    return {"ms_per_step": ms, "value": units / (ms / 1e3), "unit": UNIT,
+            "rows_scored": lay2.n_rows, "max_abs_dlogA_vs_step": float(dla.max()),
+            "step": "score (requests' rows) + assemble (carried root values) + walk + carry"}
+
+
 def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
     """Host-side tree construction (ps_build_bfs_tree, ps_predictive_allocation)
     per call through the binding, for the bench's T and request budget.  The
@@ -501,6 +570,10 @@ def main():
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(units_per_step, ws, args.steps, total_ms)
 
+    steady = None
+    if ws == 1 and getattr(w.layout, "trees", None):
+        steady = steady_state_leg(ps, w, d, dev, stream, args.steps, args.warmup)
+
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
     if not args.no_e2e:
@@ -536,6 +609,7 @@ def main():
                   "GBps": n_ch * T * 32 / (carry_ms / 1e3) / 1e9,
                   "bytes": "per position: 16 B read (row or previous value), 16 B written"},
         "tree_construction": host_tree_timing(ps, T, int(w.info.get("n_requests", 16))),
+        "steady_state": steady,
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
