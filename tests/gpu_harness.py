@@ -21,7 +21,7 @@ import torch
 
 import mh_prefetch_subtree_gb300 as ps
 import oracle
-from tests.helpers import bf16_bits
+from oracle.hostcopy import oracle_rows  # noqa: F401  (used by the tests too)
 
 TOK_RTOL = 1e-4
 TOK_ATOL = 1e-300
@@ -49,51 +49,6 @@ def run_gpu(w, per_row: bool = True, sums: bool = True, stream=None,
     out["status"] = int(out["status"][0])
     out["wstatus"] = int(out["wstatus"][0])
     return out
-
-
-def oracle_rows(w, block_rows: int = 8192, threads: int | None = None, entropy: bool = True,
-                n_rows: int | None = None):
-    """Per-row oracle values (lp0, lq, entropy), copying logits to the host
-    block by block.  entropy=False skips the entropy (returned as NaN);
-    n_rows limits the rows scored to the first n_rows (a timing sample)."""
-    n = w.n_rows if n_rows is None else min(n_rows, w.n_rows)
-    lp0 = np.empty(n)
-    lq = np.empty(n)
-    ent = np.empty(n)
-    toks = w.tokens.cpu().numpy()[:n]
-    ent[:] = np.nan
-    if w.row_index is not None:
-        # rows come from a pool: score each pool row used once per token
-        ri = w.row_index.cpu().numpy()[:n]
-        key = ri.astype(np.int64) * (w.V + 1) + toks
-        uk, inv = np.unique(key, return_inverse=True)
-        pool_rows = (uk // (w.V + 1)).astype(np.int64)
-        pool_tok = (uk % (w.V + 1)).astype(np.int32)
-        a0 = np.empty(uk.shape[0])
-        aq = np.empty(uk.shape[0])
-        ae = np.empty(uk.shape[0])
-        for i0 in range(0, uk.shape[0], block_rows):
-            i1 = min(uk.shape[0], i0 + block_rows)
-            idx = torch.from_numpy(pool_rows[i0:i1]).to(w.logits.device)
-            host = w.logits.index_select(0, idx)
-            lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
-            dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
-            res = oracle.row_logprobs(lg, dt, w.V, pool_tok[i0:i1], w.tau, threads=threads,
-                                      entropy=entropy)
-            a0[i0:i1], aq[i0:i1] = res[0], res[1]
-            ae[i0:i1] = res[2] if entropy else np.nan
-        return a0[inv], aq[inv], ae[inv]
-    for r0 in range(0, n, block_rows):
-        r1 = min(n, r0 + block_rows)
-        host = w.logits[r0:r1]
-        lg = bf16_bits(host) if host.dtype == torch.bfloat16 else host.cpu().numpy()
-        dt = "bf16" if host.dtype == torch.bfloat16 else "f32"
-        res = oracle.row_logprobs(lg, dt, w.V, toks[r0:r1], w.tau, threads=threads,
-                                  entropy=entropy)
-        lp0[r0:r1], lq[r0:r1] = res[0], res[1]
-        if entropy:
-            ent[r0:r1] = res[2]
-    return lp0, lq, ent
 
 
 def run_oracle(w, threads: int | None = None, rows=None) -> dict:

@@ -6,18 +6,7 @@ import numpy as np
 import torch
 
 
-def bf16_bits(t: torch.Tensor) -> np.ndarray:
-    """bf16 tensor -> numpy uint16 array of the same bit patterns (host copy)."""
-    assert t.dtype == torch.bfloat16
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-
-
-def logits_np(t: torch.Tensor) -> tuple[np.ndarray, str]:
-    """Host copy of a logits tensor in the form the oracle reads."""
-    if t.dtype == torch.bfloat16:
-        return bf16_bits(t), "bf16"
-    assert t.dtype == torch.float32
-    return t.detach().cpu().contiguous().numpy(), "f32"
+from oracle.hostcopy import bf16_bits, logits_np  # noqa: F401  (re-exported for the tests)
 
 
 def bf16_from_float(x: np.ndarray) -> np.ndarray:
