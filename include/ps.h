@@ -31,7 +31,11 @@
  * the caller, including the workspace.  The library allocates no device
  * memory, keeps no per-call state and is safe to call from several host
  * threads on different streams.  Calls are asynchronous on the given stream
- * (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ * (a cudaStream_t passed as void*, NULL = the legacy default stream), with
+ * plain stream order: each call sees everything enqueued on the stream before
+ * it, including the caller's own kernels that write its inputs.  (Some kernels
+ * are launched so that they start while the previous kernel finishes; they
+ * read no input before that kernel's writes are visible.)
  *
  * Errors: the returned ps_status reports what the host can check without
  * reading device memory (sizes, null pointers, alignment, launch failures).

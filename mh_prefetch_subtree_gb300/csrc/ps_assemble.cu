@@ -11,7 +11,10 @@
 //   r_i = (LQ_x - LQ_y) + alpha (LP_y - LP_x),  log A_i = min{0, r_i},
 // and, when asked, the epsilon-certainty class of the decision (section 3.3).
 //
-// One CTA per segment (a chain root only writes NaN to its own entries).  The
+// One CTA per segment (a chain root only writes NaN to its own entries).  It
+// is launched with programmatic dependent launch, so its CTAs may start while
+// the previous kernel finishes; every load of an input comes after
+// griddepcontrol.wait, which makes all of that kernel's writes visible.  The
 // threads stride over the rows in float64 and the block reduces in a fixed
 // order (warp butterfly, then warps in index order), so results are
 // bit-reproducible.  Every index is checked before use; a failing request
@@ -99,6 +102,10 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     const int warp = tid >> 5;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
     pdl_launch_dependents();                         // the walk may be scheduled now
+    // Wait for the previous kernel in the stream before reading anything: the
+    // per-row values come from the scoring kernel, and the caller may have
+    // written the layout arrays with a kernel just before this call.
+    pdl_wait_prerequisites();
     const int c = chain_of(p.chain_seg0, p.n_chains, s);
     // metadata in two rounds of loads: what depends on s (and c) only, then
     // the root's and src's entries (indices clamped in range, checked below)
@@ -154,7 +161,6 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     if (bits == 0 && (cs > csrc || (cs < rc && p.root_lp0 == nullptr))) bits |= PS_DEV_INFEASIBLE;
 
     double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
-    pdl_wait_prerequisites();                        // per-row values are now visible
     if (bits == 0) {                                 // uniform across the block
         double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
         // y: the request's own rows.  x: positions cs+1..csrc of the current

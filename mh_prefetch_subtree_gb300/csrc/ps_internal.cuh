@@ -108,10 +108,11 @@ struct WalkParams {
     int32_t *status;
 };
 
-// Launchers (host side, asynchronous on `stream`).  The assemble and walk
-// kernels are launched with programmatic stream serialization, so each may
-// start while its predecessor in the stream finishes; they wait
-// (griddepcontrol.wait) before reading anything that predecessor writes.
+// Launchers (host side, asynchronous on `stream`).  The assemble, walk and
+// carry kernels are launched with programmatic stream serialization, so each
+// may start while its predecessor in the stream finishes; they wait
+// (griddepcontrol.wait) before their first load of any input, because the
+// predecessor may be the caller's own kernel writing those inputs.
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream);
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);

@@ -57,6 +57,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
     const int stride = p.max_steps + 1;
     int32_t *path = p.path ? p.path + (int64_t)c * stride : nullptr;
 
+    // Launched with programmatic dependent launch: wait for the previous
+    // kernel in the stream before any load, since log A comes from it and the
+    // caller may have written the tree or the uniforms with a kernel just
+    // before this call.
+    pdl_wait_prerequisites();
     const int32_t n0 = p.chain_node0[c], n1 = p.chain_node0[c + 1];
     const int32_t s0 = p.chain_seg0[c], s1 = p.chain_seg0[c + 1];
     if (n0 < 0 || n1 > p.n_nodes || n1 <= n0 || s0 < 0 || s1 > p.n_seg || s1 <= s0) {
@@ -81,7 +86,6 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const WalkParams 
         }
         for (int i = lane; i < ns; i += 32) w.u[i] = p.u[s0 + i];
     }
-    pdl_wait_prerequisites();          // log A from the scoring kernels is now visible
     if (staged) {
         // each request's decision, taken by all lanes at once so that the walk
         // below only follows it
