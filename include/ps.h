@@ -306,10 +306,11 @@ ps_status ps_carry_state(const ps_subtree_batch *batch, const ps_carry_io *io,
  * routine.  Inputs and outputs are the caller's, exactly as in
  * ps_score_subtree.
  *
- * Limit: when out->lp0 or out->lq is NULL, the per-row values are kept in the
- * static array, which holds at most 262144 rows; a larger batch returns
- * PS_ERR_WORKSPACE without launching anything.  With both lp0 and lq supplied
- * there is no row limit.
+ * Limit: a per-row array the caller leaves NULL (out->lp0, out->lq, or both)
+ * is kept in the static array instead, which holds at most 262144 rows of
+ * each; a larger batch then returns PS_ERR_WORKSPACE without launching
+ * anything.  Whichever of lp0 and lq the caller supplies is written, as in
+ * ps_score_subtree; with both supplied there is no row limit.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture.
@@ -433,7 +434,6 @@ ps_status ps_predictive_allocation(int32_t n_nodes, const int32_t *acc, const in
 /* eq. (14): h(v+) = (1 + P(certain accept) - P(certain reject)) / 2 (Lemma 3). */
 double ps_midpoint_branch_probability(double p_accept, double p_reject);
 
-/* Static text for a status code. */
 /*
  * Diagnostic with no counterpart in the PreSTO pages: checks on the device the
  * bounded wait that every bulk-copy wait of the scoring kernel uses.  One warp
@@ -448,6 +448,7 @@ double ps_midpoint_branch_probability(double p_accept, double p_reject);
  */
 ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status, void *cuda_stream);
 
+/* Static text for a status code. */
 const char *ps_status_string(ps_status status);
 
 /* Library version string. */

@@ -132,23 +132,25 @@ size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
 
 namespace {
 
-// Shared launch of the row kernel.  npow/g select the tau path; for the
-// multi-temperature mode (npow == 16) taus_pow/n_taus/lq_multi replace lq.
-ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
-                            double *entropy, int32_t *status, void *workspace,
-                            size_t workspace_bytes, void *cuda_stream, int32_t npow, float g,
-                            const int32_t *tau_pow, int32_t n_taus, double *lq_multi) {
-    const WsLayout wl = ws_layout(b->n_rows);
-    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
-        return PS_ERR_WORKSPACE;
-    if (b->n_rows == 0) return PS_OK;
-    int sms = 0;
-    ps_status st = device_of(b->logits, &sms);
-    if (st != PS_OK) return st;
+// Where the row kernel keeps its scratch: the split-row partials, the arrival
+// counters, and how many warps (one partial pair and one counter each) fit.
+struct RowsScratch {
+    ps::RowPart *parts;
+    int32_t *counters;
+    int64_t max_warps;
+};
+
+// Launch of the row kernel shared by every scoring entry point.  npow/g select
+// the tau path; for the multi-temperature mode (npow == 16 or 17)
+// tau_pow/n_taus/lq_multi replace lq.  The batch has been checked by
+// check_batch_host and has at least one row.
+ps_status launch_rows(const ps_subtree_batch *b, int sms, const RowsScratch &scr, double *lp0,
+                      double *lq, double *entropy, int32_t *status, void *cuda_stream,
+                      int32_t npow, float g, const int32_t *tau_pow, int32_t n_taus,
+                      double *lq_multi) {
     cudaStream_t stream = (cudaStream_t)cuda_stream;
-    uint8_t *ws = (uint8_t *)workspace;
     const int esz = elem_size(b->dtype);
-    ps::RowsParams p;
+    ps::RowsParams p{};
     p.logits = (const uint8_t *)b->logits;
     p.ld_bytes = b->ld * esz;
     p.n_logit_rows = b->row_index ? b->n_logit_rows : b->n_rows;
@@ -162,7 +164,7 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
     p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
     p.n_chunks = b->n_rows * p.cpr;
     int64_t warps = (int64_t)sms * ps::kWarpsPerCta;
-    if (warps > ps::kMaxWarps) warps = ps::kMaxWarps;
+    if (warps > scr.max_warps) warps = scr.max_warps;
     if (warps > p.n_chunks) warps = p.n_chunks;
     p.n_vwarps = (int32_t)warps;
     p.npow = npow;
@@ -173,13 +175,34 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
     p.lp0 = lp0;
     p.lq = lq;
     p.entropy = entropy;
-    p.parts = (ps::RowPart *)(ws + wl.parts_off);
-    p.counters = (int32_t *)(ws + wl.cnt_off);
+    p.parts = scr.parts;
+    p.counters = scr.counters;
     p.status = status;
     const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
-    st = map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
+    // the counters must start at zero whatever the scratch held before
+    ps_status st =
+        map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
     if (st != PS_OK) return st;
     return map_cuda(ps::launch_score_rows(p, n_ctas, stream));
+}
+
+// The row kernel on a caller workspace.
+ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
+                            double *entropy, int32_t *status, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream, int32_t npow, float g,
+                            const int32_t *tau_pow, int32_t n_taus, double *lq_multi) {
+    const WsLayout wl = ws_layout(b->n_rows);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
+        return PS_ERR_WORKSPACE;
+    if (b->n_rows == 0) return PS_OK;
+    int sms = 0;
+    ps_status st = device_of(b->logits, &sms);
+    if (st != PS_OK) return st;
+    uint8_t *ws = (uint8_t *)workspace;
+    const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), (int32_t *)(ws + wl.cnt_off),
+                          ps::kMaxWarps};
+    return launch_rows(b, sms, scr, lp0, lq, entropy, status, cuda_stream, npow, g, tau_pow,
+                       n_taus, lq_multi);
 }
 
 }  // namespace
@@ -477,8 +500,9 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     if (st != PS_OK) return st;
     if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
     if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
-    const bool rows_in_scratch = out->lp0 == nullptr || out->lq == nullptr;
-    if (rows_in_scratch && b->n_rows > kNoAllocMaxRows) return PS_ERR_WORKSPACE;
+    // a per-row array the caller does not supply is kept in the static array
+    const bool lp0_scratch = out->lp0 == nullptr, lq_scratch = out->lq == nullptr;
+    if ((lp0_scratch || lq_scratch) && b->n_rows > kNoAllocMaxRows) return PS_ERR_WORKSPACE;
     int sms = 0;
     st = device_of(b->n_rows > 0 ? b->logits : out->log_accept, &sms);
     if (st != PS_OK) return st;
@@ -487,42 +511,14 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     uint8_t *base = nullptr;
     st = noalloc_scratch(dev, &base);
     if (st != PS_OK) return st;
-    cudaStream_t stream = (cudaStream_t)cuda_stream;
-    double *lp0 = rows_in_scratch ? (double *)base : out->lp0;
-    double *lq = rows_in_scratch ? (double *)base + kNoAllocMaxRows : out->lq;
-
+    double *lp0 = lp0_scratch ? (double *)base : out->lp0;
+    double *lq = lq_scratch ? (double *)base + kNoAllocMaxRows : out->lq;
     if (b->n_rows > 0) {
-        const int esz = elem_size(b->dtype);
-        ps::RowsParams p;
-        p.logits = (const uint8_t *)b->logits;
-        p.ld_bytes = b->ld * esz;
-        p.n_logit_rows = b->row_index ? b->n_logit_rows : b->n_rows;
-        p.row_index = b->row_index;
-        p.tokens = b->tokens;
-        p.n_rows = b->n_rows;
-        p.V = b->V;
-        p.dtype = b->dtype;
-        p.flags = b->flags;
-        p.row_bytes = (int32_t)(((int64_t)b->V * esz + 15) / 16 * 16);
-        p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
-        p.n_chunks = b->n_rows * p.cpr;
-        int64_t warps = (int64_t)sms * ps::kWarpsPerCta;
-        if (warps > kNoAllocMaxWarps) warps = kNoAllocMaxWarps;   // fits the array
-        if (warps > p.n_chunks) warps = p.n_chunks;
-        p.n_vwarps = (int32_t)warps;
-        p.npow = integer_power(b->tau);
-        p.g = (float)(1.0 / b->tau);
-        p.lp0 = lp0;
-        p.lq = lq;
-        p.entropy = out->entropy;
-        p.parts = (ps::RowPart *)(base + kNoAllocRowBytes);
-        p.counters = (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes);
-        p.status = out->status;
-        const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
-        // the counters must start at zero: the array keeps the last call's contents
-        st = map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
-        if (st != PS_OK) return st;
-        st = map_cuda(ps::launch_score_rows(p, n_ctas, stream));
+        const RowsScratch scr{(ps::RowPart *)(base + kNoAllocRowBytes),
+                              (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes),
+                              kNoAllocMaxWarps};
+        st = launch_rows(b, sms, scr, lp0, lq, out->entropy, out->status, cuda_stream,
+                         integer_power(b->tau), (float)(1.0 / b->tau), nullptr, 0, nullptr);
         if (st != PS_OK) return st;
     }
     return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
