@@ -4,13 +4,20 @@ One step = the whole hot path over one subtree batch already resident in HBM:
 per-token log p0 / log q_tau of every row (ps_score_rows), suffix sums and
 log A per request (ps_assemble_subtree), and the walk (ps_walk_subtree).
 
-Default workload: Qwen3-like vocabulary V = 151936 bf16, T = 1024,
-N_pf = 16 BFS, alpha = 4, tau = 0.25 (about 13.7k rows, 4.2 GB of logits,
-far larger than the 129 MB L2, so no flush is needed between steps).
+Default workload: the long-context batch, the largest of the five
+configurations that a single GPU holds: Qwen3-like vocabulary V = 151936
+bf16, T = 3072, N_pf = 64 requests in a unary-heavy subtree (spine of depth
+30), alpha = 4, tau = 0.25; 98,469 rows, 95,486 scored suffix tokens and
+29.9 GB of logits, far larger than the 129 MB L2, so no flush is needed
+between steps.
 
 metric  scored suffix tokens per second (sum over requests of T - c_i,
         whole job over all ranks); logits GB/s and the HBM roofline of the
-        scoring kernel are reported alongside.
+        scoring kernel are reported alongside.  The line also carries the
+        scoring kernel's other variants, the end-to-end rate from host
+        buffers, the CPU oracle on the same batch, and the 36-point throughput
+        sweep (256 chains per point, rows read through a shuffled row index
+        into a pool of distinct rows sized far above the L2).
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank scores its own batch (independent problems, weak
 scaling, no collective on the data path).
@@ -38,10 +45,11 @@ METRIC = "scored suffix tokens/sec and logits GB/s vs GB300 HBM peak per subtree
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
-# DRAM bytes per launch of the scoring kernel on the default workload, from one
-# ncu capture (profiles/score_rows_config2_launches.md), valid for this source hash.
+# DRAM bytes (read + write) per launch of the scoring kernel on the default
+# workload, from one ncu capture of this kernel code (identified by its hash).
 NCU_TRAFFIC = {"source_sha1": "726286a81d5ed43f45d983e626b4d6049846d235",
-               "bytes_per_launch": 4160389120 + 3825920, "config": 2}
+               "bytes_per_launch": 29923933440 + 7622912, "config": 3}
+GENERAL_TAU = 0.3                   # a temperature whose 1/tau is not 1, 2, 4 or 8
 
 
 def log(*a):
@@ -196,7 +204,7 @@ def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
     explicit states, log A and the walk, on all host cores; and the per-row
     part on one core over a sample of rows, extrapolated to the batch."""
     import oracle
-    from tests.gpu_harness import oracle_rows   # block-wise host copies for the oracle
+    from oracle.hostcopy import oracle_rows     # block-wise host copies for the oracle
     threads = oracle.default_threads()
     lay = w.layout
     units = lay.suffix_tokens()
@@ -235,17 +243,22 @@ def reference_arm(args, ws, rank):
     from synth import make_workload
     from synth.trees import assemble_layout
     w = make_workload(args.config, device="cpu") if args.config == 1 else None
+    tokens_per_row = None               # of the full batch, when w is a sample of it
     if w is None:
-        # a bounded sample of the same batch: the same trees, with the rows of
-        # the first requests only (root rows + enough requests for ~1 s of work)
+        # a bounded sample of the same batch: the same tree, with the root's
+        # rows and the rows of its first requests only (at least one request,
+        # and up to 2,500 request rows: about a second of oracle work)
         from synth.workload import CONFIGS, _trees_for, draw_tokens, gen_logits, Workload
         cfg = dict(CONFIGS[args.config])
         rng = np.random.default_rng(10086 + args.config)
         tree = _trees_for(cfg, rng)[0]
+        full = assemble_layout([tree])
+        tokens_per_row = full.suffix_tokens() / full.n_rows
         keep = 1
-        rows = tree.T - tree.seg_cut[0]
-        while keep < len(tree.seg_cut) and rows + tree.T - tree.seg_cut[keep] <= 2500:
-            rows += tree.T - tree.seg_cut[keep]
+        req_rows = 0
+        while keep < len(tree.seg_cut) and (
+                keep == 1 or req_rows + tree.T - tree.seg_cut[keep] <= 2500):
+            req_rows += tree.T - tree.seg_cut[keep]
             keep += 1
         tree.seg_cut = tree.seg_cut[:keep]
         tree.seg_src = tree.seg_src[:keep]
@@ -257,7 +270,7 @@ def reference_arm(args, ws, rank):
         w = Workload(name=cfg["name"], layout=lay, V=cfg["V"], dtype=cfg["dtype"],
                      alpha=cfg["alpha"], tau=cfg["tau"], logits=x, tokens=tok,
                      u=1.0 - rng.random(lay.n_seg), max_steps=cfg["max_steps"])
-    from tests.helpers import logits_np
+    from oracle.hostcopy import logits_np
     lg, dt = logits_np(w.logits)
     toks = w.tokens.numpy()
     threads = oracle.default_threads()
@@ -272,81 +285,119 @@ def reference_arm(args, ws, rank):
     for _ in range(args.steps):
         step()
     el = time.time() - t0
-    units = w.layout.suffix_tokens() * args.steps
-    v = units / el
+    # The oracle's time is proportional to the rows it scores.  A sample keeps
+    # all of the root's rows, so it holds more root rows per request row than
+    # the batch; each sampled row is credited with the batch's suffix tokens
+    # per row, so that the rate is the one the whole batch would give.
+    if tokens_per_row is None:
+        units_per_step = w.layout.suffix_tokens()
+        how = f"the whole batch ({w.n_rows} rows) per step"
+    else:
+        units_per_step = w.n_rows * tokens_per_row
+        how = (f"{w.n_rows} rows of the batch per step (the root's and its first requests'); "
+               f"tokens = rows x the batch's {tokens_per_row:.4f} suffix tokens per row")
+    v = units_per_step * args.steps / el
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "sample_rows": w.n_rows,
-                       "sample_suffix_tokens": w.layout.suffix_tokens()},
+                       "sample_suffix_tokens": w.layout.suffix_tokens(),
+                       "credited_tokens_per_step": units_per_step},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{w.n_rows} rows of the batch per step"},
+                             "sample": how},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def sweep(args) -> int:
-    """--sweep: the throughput sweep (256 independent chains x N_pf x T x alpha,
-    tau = 1/alpha, rows read through a shuffled row index into a pool of 8192
-    distinct rows, 2.5 GB > L2).  Prints one JSON line per point and one with
-    the aggregate; informative, not the bench line."""
-    import __graft_entry__
-    __graft_entry__.build()
-    import mh_prefetch_subtree_gb300 as ps
-    from synth.workload import SWEEP5, make_pool, workload_config5
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+def sweep_leg(ps, dev, stream, steps: int, warmup: int, per_point: bool = False,
+              max_points: int | None = None) -> dict:
+    """The throughput sweep: at each of the 36 points (N_pf x T x alpha, tau =
+    1/alpha) 256 independent chains, their rows read through a shuffled row
+    index into a pool of distinct logits rows of at least 16 GB and 128 x the
+    L2 size, so that the reads come from DRAM.  Each point's step (score,
+    assemble, walk) and its scoring kernel alone are timed with CUDA events;
+    the aggregate is the sum of tokens (and logits bytes) over the sum of
+    times.  per_point prints one JSON line per point as well."""
+    from synth.workload import SWEEP5, make_pool, sweep_pool_rows, workload_config5
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_pool = sweep_pool_rows(SWEEP5["V"], 2, l2)
     taus = [1.0 / a for a in SWEEP5["alpha"]]
-    pool, ptok = make_pool(8192, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus, seed=10091,
+    pool, ptok = make_pool(n_pool, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus, seed=10091,
                            device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    tot_tokens, tot_ms, tot_bytes, tot_k1 = 0, 0.0, 0.0, 0.0
+    tot = dict(tokens=0, rows=0, ms=0.0, k1_ms=0.0, bytes=0)
+    points = []
     for n_pf in SWEEP5["n_pf"]:
         for T in SWEEP5["T"]:
             for alpha in SWEEP5["alpha"]:
+                if max_points is not None and len(points) >= max_points:
+                    break
                 w = workload_config5(pool, ptok, n_pf, T, alpha, n_chains=256)
                 d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits,
                                             tokens=w.tokens, V=w.V, alpha=w.alpha, tau=w.tau,
                                             max_steps=w.max_steps, row_index=w.row_index)
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 with torch.cuda.stream(stream):
-                    for _ in range(args.warmup):
+                    for _ in range(warmup):
                         d.score_rows(stream), d.assemble(stream), d.walk(stream)
-                    torch.cuda.synchronize()
                     ev[0].record(stream)
-                    for _ in range(args.sweep_steps):
+                    for _ in range(steps):
                         d.score_rows(stream), d.assemble(stream), d.walk(stream)
                     ev[1].record(stream)
                     ev[2].record(stream)
-                    for _ in range(args.sweep_steps):
+                    for _ in range(steps):
                         d.score_rows(stream)
                     ev[3].record(stream)
                 torch.cuda.synchronize()
                 st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
                 assert st == 0, ps.dev_status_names(st)
-                ms = ev[0].elapsed_time(ev[1]) / args.sweep_steps
-                k1 = ev[2].elapsed_time(ev[3]) / args.sweep_steps
+                ms = ev[0].elapsed_time(ev[1]) / steps
+                k1 = ev[2].elapsed_time(ev[3]) / steps
                 units = w.layout.suffix_tokens()
                 nbytes = w.n_rows * w.V * 2
-                tot_tokens += units
-                tot_ms += ms
-                tot_bytes += nbytes
-                tot_k1 += k1
-                print(json.dumps({"sweep_point": {"n_pf": n_pf, "T": T, "alpha": alpha,
-                                                  "rows": w.n_rows, "suffix_tokens": units,
-                                                  "ms_per_step": ms, "tokens_per_s": units / ms * 1e3,
-                                                  "k1_ms": k1,
-                                                  "logits_GBps": nbytes / k1 / 1e6}}), flush=True)
+                tot["tokens"] += units
+                tot["rows"] += w.n_rows
+                tot["ms"] += ms
+                tot["k1_ms"] += k1
+                tot["bytes"] += nbytes
+                pt = {"n_pf": n_pf, "T": T, "alpha": alpha, "rows": w.n_rows,
+                      "suffix_tokens": units, "ms_per_step": ms,
+                      "tokens_per_s": units / ms * 1e3, "k1_ms": k1,
+                      "logits_GBps": nbytes / k1 / 1e6}
+                points.append(pt)
+                if per_point:
+                    print(json.dumps({"sweep_point": pt}), flush=True)
                 del d, w
-    print(json.dumps({"sweep": {"points": len(SWEEP5["n_pf"]) * len(SWEEP5["T"]) *
-                                len(SWEEP5["alpha"]), "n_chains": 256,
-                                "tokens_per_s": tot_tokens / tot_ms * 1e3,
-                                "logits_GBps": tot_bytes / tot_k1 / 1e6,
-                                "note": "each point's step timed alone; totals over all points"}}),
-          flush=True)
+    del pool, ptok
+    torch.cuda.empty_cache()
+    rates = [p["tokens_per_s"] for p in points]
+    gbps = [p["logits_GBps"] for p in points]
+    return {"points": len(points), "n_chains": 256,
+            "pool_rows": n_pool, "pool_bytes": n_pool * SWEEP5["V"] * 2, "l2_bytes": l2,
+            "tokens_per_s": tot["tokens"] / tot["ms"] * 1e3,
+            "rows": tot["rows"], "suffix_tokens": tot["tokens"],
+            "logits_GBps": tot["bytes"] / tot["k1_ms"] / 1e6,
+            "frac_of_8TBps": tot["bytes"] / tot["k1_ms"] / 1e6 / NOMINAL_HBM_GBS,
+            "tokens_per_s_range": [min(rates), max(rates)],
+            "logits_GBps_range": [min(gbps), max(gbps)],
+            "steps_per_point": steps,
+            "note": "each point's step and scoring kernel timed alone; totals over all points"}
+
+
+def sweep(args) -> int:
+    """--sweep: the throughput sweep alone, one JSON line per point and one
+    with the aggregate (the default bench line carries the aggregate too)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import mh_prefetch_subtree_gb300 as ps
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    agg = sweep_leg(ps, dev, stream, args.sweep_steps, max(1, args.sweep_warmup), per_point=True,
+                    max_points=args.sweep_points)
+    print(json.dumps({"sweep": agg}), flush=True)
     return 0
 
 
@@ -446,19 +497,39 @@ def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
             "where": "host, per call through the binding"}
 
 
+def kernel_loop(stream, steps: int, fn) -> float:
+    """Average device time (ms) of fn() over `steps` back-to-back calls on
+    `stream`, from CUDA events recorded on that stream."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="libps", choices=["libps", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave the 36-point throughput sweep out of the bench line")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the step and the scoring kernel (for profiling runs)")
     ap.add_argument("--sweep", action="store_true",
-                    help="time the 36-point throughput sweep instead (informative)")
-    ap.add_argument("--sweep-steps", type=int, default=5)
+                    help="time the 36-point throughput sweep alone, one line per point")
+    ap.add_argument("--sweep-steps", type=int, default=2)
+    ap.add_argument("--sweep-warmup", type=int, default=1)
+    ap.add_argument("--sweep-points", type=int, default=None,
+                    help="with --sweep: time only the first K points (for profiling runs)")
     ap.add_argument("--n-pf", type=int, default=None,
                     help="override the request budget (smaller batches for profiling)")
     args = ap.parse_args()
@@ -491,32 +562,19 @@ def main():
     logits_bytes = w.logits_bytes()
     alg_bytes_k1 = rows * (w.V * w.elem_bytes + 4 + 16)   # logits + token in, lp0/lq out
 
+    def step():
+        d.score_rows(stream)
+        d.assemble(stream)
+        d.walk(stream)
+
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            d.score_rows(stream)
-            d.assemble(stream)
-            d.walk(stream)
+            step()
     torch.cuda.synchronize()
     st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
     assert st == 0, ps.dev_status_names(st)
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k1a, k1b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k1c, k1d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ent_rows = torch.empty(w.n_rows, dtype=torch.float64, device=dev)
-    mt_taus = [0.25, 0.5, 1.0]          # MultiTryMH candidate temperatures
-    mt_lq = torch.empty((len(mt_taus), w.n_rows), dtype=torch.float64, device=dev)
-    k1e, k1f = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cy_a, cy_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_ch, T = lay.n_chains, lay.T
-    cy_out = {k: torch.empty((n_ch, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
-    cy_prev = {k: torch.zeros((n_ch, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
-    cy_ll = torch.empty(n_ch, dtype=torch.float64, device=dev)
-    cy_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    carry_io = ps.make_carry_io(state_seg=d.t["state_seg"], row_lp0=d.t["lp0"], row_lq=d.t["lq"],
-                                prev_lp0=cy_prev["lp0"], prev_lq=cy_prev["lq"],
-                                next_lp0=cy_out["lp0"], next_lq=cy_out["lq"], loglik=cy_ll,
-                                status=cy_status)
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -528,51 +586,29 @@ def main():
         # each kernel's launch overlaps the tail of the one before it
         start.record(stream)
         for _ in range(args.steps):
-            d.score_rows(stream)
-            d.assemble(stream)
-            d.walk(stream)
+            step()
         end.record(stream)
-        # the scoring kernel alone, back to back, for its roofline
-        k1a.record(stream)
-        for _ in range(args.steps):
-            d.score_rows(stream)
-        k1b.record(stream)
-        # and its variant that also returns the entropy of p0 per row
-        k1c.record(stream)
-        for _ in range(args.steps):
-            ps.ps_score_rows(d.batch, d.t["lp0"], d.t["lq"], d.t["status"], d.workspace,
-                             stream, entropy=ent_rows)
-        k1d.record(stream)
-        # the round carry-over (reached state's per-position values) after a step
-        cy_a.record(stream)
-        for _ in range(args.steps):
-            ps.ps_carry_state(d.batch, carry_io, stream)
-        cy_b.record(stream)
-        # and the multi-temperature variant (log q at all three temperatures)
-        k1e.record(stream)
-        for _ in range(args.steps):
-            ps.ps_score_rows_multi(d.batch, mt_taus, d.t["lp0"], mt_lq, d.t["status"],
-                                   d.workspace, stream)
-        k1f.record(stream)
     torch.cuda.synchronize()
+    # the scoring kernel alone, back to back on the same stream, for its roofline
+    k1_avg = kernel_loop(stream, args.steps, lambda: d.score_rows(stream))
     clocks.mark(False)
     if ws > 1:
         torch.distributed.barrier()
-    clocks.stop()
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
-    k1_avg = k1a.elapsed_time(k1b) / args.steps
-    k1_ent_avg = k1c.elapsed_time(k1d) / args.steps
-    k1_mt_avg = k1e.elapsed_time(k1f) / args.steps
-    carry_ms = cy_a.elapsed_time(cy_b) / args.steps
-    assert int(cy_status.item()) == 0, ps.dev_status_names(int(cy_status.item()))
-    st = int(d.t["status"].item())
+    st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
     assert st == 0, ps.dev_status_names(st)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(units_per_step, ws, args.steps, total_ms)
 
-    steady = None
-    if ws == 1 and getattr(w.layout, "trees", None):
-        steady = steady_state_leg(ps, w, d, dev, stream, args.steps, args.warmup)
+    extras = {}
+    if not args.no_extras:
+        extras = variant_legs(ps, w, d, dev, stream, args.steps, logits_bytes)
+        n_ch, T = lay.n_chains, lay.T
+        extras["tree_construction"] = host_tree_timing(ps, T, int(w.info.get("n_requests", 16)))
+        if ws == 1 and getattr(w.layout, "trees", None):
+            extras["steady_state"] = steady_state_leg(ps, w, d, dev, stream, args.steps,
+                                                      args.warmup)
+    clocks.stop()
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
@@ -589,7 +625,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic (seeded logits, BFS trees, proposal tokens drawn from q_tau)",
+        "data": "synthetic (seeded logits, trees of the configuration's rule, proposal tokens "
+                "drawn from q_tau)",
         "config": {"workload": w.name, "V": w.V, "T": lay.T, "n_requests": lay.n_seg - lay.n_chains,
                    "rows": rows, "suffix_tokens": units_per_step, "logits_bytes": logits_bytes,
                    "alpha": w.alpha, "tau": w.tau,
@@ -597,19 +634,12 @@ def main():
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "peak_source": f"{peak_src} hbm_gbs (a read+write copy; a read-only "
+                                    "stream can exceed it)",
                      "kernel": "score_rows_kernel", "kernel_ms": k1_avg,
+                     "algorithmic_bytes": alg_bytes_k1,
                      "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
-        "with_entropy": {"kernel_ms": k1_ent_avg,
-                         "logits_GBps": logits_bytes / (k1_ent_avg / 1e3) / 1e9},
-        "multi_temperature": {"taus": mt_taus, "kernel_ms": k1_mt_avg,
-                              "logits_GBps": logits_bytes / (k1_mt_avg / 1e3) / 1e9},
-        "carry": {"kernel_ms": carry_ms,
-                  "GBps": n_ch * T * 32 / (carry_ms / 1e3) / 1e9,
-                  "bytes": "per position: 16 B read (row or previous value), 16 B written"},
-        "tree_construction": host_tree_timing(ps, T, int(w.info.get("n_requests", 16))),
-        "steady_state": steady,
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 3 * args.steps,
         "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
@@ -618,15 +648,67 @@ def main():
         "after_scoring_us": (ms_per_step - k1_avg) * 1e3,
         "clocks": clocks.summary(),
     }
+    line.update(extras)
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0 and ws == 1 and not args.no_sweep:
+        del d, w
+        torch.cuda.empty_cache()
+        line["sweep"] = sweep_leg(ps, dev, stream, args.sweep_steps, args.sweep_warmup)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def variant_legs(ps, w, d, dev, stream, steps: int, logits_bytes: int) -> dict:
+    """The scoring kernel's other variants on the same batch, each timed back
+    to back on the bench stream: with the entropy of p0, at three temperatures
+    in one pass, at a temperature whose 1/tau is not an integer (a second
+    exponential per logit), that with the entropy; and the round carry-over."""
+    n = w.n_rows
+    f64 = lambda *shape: torch.empty(shape, dtype=torch.float64, device=dev)
+    ent_rows, lp0_v, lq_v = f64(n), f64(n), f64(n)
+    mt_taus = [0.25, 0.5, 1.0]          # MultiTryMH candidate temperatures
+    mt_lq = f64(len(mt_taus), n)
+    bg = type(d.batch).from_buffer_copy(d.batch)
+    bg.tau = GENERAL_TAU
+    bg._keep = d.batch._keep
+    rate = lambda ms: {"kernel_ms": ms, "logits_GBps": logits_bytes / (ms / 1e3) / 1e9,
+                       "frac_of_8TBps": logits_bytes / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS}
+    out = {}
+    out["with_entropy"] = rate(kernel_loop(stream, steps, lambda: ps.ps_score_rows(
+        d.batch, lp0_v, lq_v, d.t["status"], d.workspace, stream, entropy=ent_rows)))
+    out["multi_temperature"] = dict(taus=mt_taus, **rate(kernel_loop(
+        stream, steps, lambda: ps.ps_score_rows_multi(d.batch, mt_taus, lp0_v, mt_lq,
+                                                      d.t["status"], d.workspace, stream))))
+    out["general_tau"] = dict(tau=GENERAL_TAU, **rate(kernel_loop(
+        stream, steps, lambda: ps.ps_score_rows(bg, lp0_v, lq_v, d.t["status"], d.workspace,
+                                                stream))))
+    out["general_tau_with_entropy"] = dict(tau=GENERAL_TAU, **rate(kernel_loop(
+        stream, steps, lambda: ps.ps_score_rows(bg, lp0_v, lq_v, d.t["status"], d.workspace,
+                                                stream, entropy=ent_rows))))
+    st = int(d.t["status"].item())
+    assert st == 0, ps.dev_status_names(st)
+    # the round carry-over (reached state's per-position values) after a step
+    lay = w.layout
+    n_ch, T = lay.n_chains, lay.T
+    cy_out = {k: f64(n_ch, T) for k in ("lp0", "lq")}
+    cy_prev = {k: torch.zeros((n_ch, T), dtype=torch.float64, device=dev) for k in ("lp0", "lq")}
+    cy_ll = f64(n_ch)
+    cy_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    io = ps.make_carry_io(state_seg=d.t["state_seg"], row_lp0=d.t["lp0"], row_lq=d.t["lq"],
+                          prev_lp0=cy_prev["lp0"], prev_lq=cy_prev["lq"],
+                          next_lp0=cy_out["lp0"], next_lq=cy_out["lq"], loglik=cy_ll,
+                          status=cy_status)
+    carry_ms = kernel_loop(stream, steps, lambda: ps.ps_carry_state(d.batch, io, stream))
+    assert int(cy_status.item()) == 0, ps.dev_status_names(int(cy_status.item()))
+    out["carry"] = {"kernel_ms": carry_ms, "GBps": n_ch * T * 32 / (carry_ms / 1e3) / 1e9,
+                    "bytes": "per position: 16 B read (row or previous value), 16 B written"}
+    return out
 
 
 def e2e_leg(ps, w, d, dev, stream, args, ws, chunks: int = 8):

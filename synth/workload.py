@@ -194,6 +194,20 @@ def make_workload(k: int, device="cpu", **override) -> Workload:
                               n_requests=layout.n_seg - layout.n_chains))
 
 
+SWEEP5_POOL_MIN_BYTES = 16 * 10**9     # distinct rows the sweep reads through its row index
+SWEEP5_POOL_L2_MULT = 128              # and at least this many times the L2 cache
+
+
+def sweep_pool_rows(V: int, elem_bytes: int, l2_bytes: int,
+                    min_bytes: int = SWEEP5_POOL_MIN_BYTES) -> int:
+    """Distinct logits rows in the pool of configuration 5: at least
+    ``min_bytes`` and ``SWEEP5_POOL_L2_MULT`` x the L2 size, so that rows read in
+    a shuffled order come from DRAM, not from the L2 cache."""
+    row = -(-V * elem_bytes // 16) * 16
+    need = max(int(min_bytes), SWEEP5_POOL_L2_MULT * int(l2_bytes))
+    return -(-need // row)
+
+
 def make_pool(n_pool: int, V: int, dtype: str, params: dict, taus, seed: int,
               device="cpu"):
     """A pool of distinct logits rows and one proposal token per (row, tau)."""

@@ -13,7 +13,8 @@ import mh_prefetch_subtree_gb300 as ps
 import oracle
 from synth import make_workload
 from synth.trees import assemble_layout, bfs_tree
-from synth.workload import SWEEP5, Workload, draw_tokens, gen_logits, make_pool, workload_config5
+from synth.workload import (SWEEP5, Workload, draw_tokens, gen_logits, make_pool,
+                             sweep_pool_rows, workload_config5)
 from tests import gpu_harness as H
 from tests.helpers import bf16_bits
 
@@ -62,11 +63,13 @@ def test_config4_full():
 
 @pytest.fixture(scope="module")
 def sweep_pool():
-    """The row pool of configuration 5 and the oracle's per-row values of every
-    pool row at each sweep temperature (tokens are drawn per (row, tau), so a
-    scored row's values depend only on its pool row and tau)."""
+    """The row pool of configuration 5, as the bench builds it (at least 16 GB
+    of distinct rows and 128 x the L2 size), and the oracle's per-row values of
+    every pool row at each sweep temperature (tokens are drawn per (row, tau),
+    so a scored row's values depend only on its pool row and tau)."""
     taus = [1.0 / a for a in SWEEP5["alpha"]]
-    pool, ptok = make_pool(8192, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus,
+    n_pool = sweep_pool_rows(SWEEP5["V"], 2, torch.cuda.get_device_properties(DEV).L2_cache_size)
+    pool, ptok = make_pool(n_pool, SWEEP5["V"], "bf16", SWEEP5["logits"][1], taus,
                            seed=10091, device=DEV)
     lg = bf16_bits(pool)
     vals = {}
