@@ -127,11 +127,13 @@ struct Acc {
 
 __device__ __forceinline__ Acc acc_empty() { return Acc{-INFINITY, 0.f, {0.f, 0.f, 0.f}, 0.f}; }
 
-// One pair of logits: accumulate 2^x into a1, 2^(g x) into at[0] (or the three
-// power sums into at[0..2]) and 2^x x into ay.
+// One pair of logits v: accumulate 2^x into a1, 2^(g x) into at[0] (or the
+// three power sums into at[0..2]) and 2^x x into ay, with x = v L - R.  For a
+// general g the tau exponent g x = v (g L) - g R is formed from v directly
+// (GL2, nGR2), so that it does not wait for x.
 template <int NP, bool ENT>
-__device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2, float2 &a1,
-                                      float2 (&at)[3], float2 &ay) {
+__device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 GL2, float2 nGR2,
+                                      float2 &a1, float2 (&at)[3], float2 &ay) {
     const float2 x = __ffma2_rn(v, L2, nR2);
     const float2 e = make_float2(ex2(x.x), ex2(x.y));
     a1 = __fadd2_rn(a1, e);
@@ -152,7 +154,7 @@ __device__ __forceinline__ void step2(float2 v, float2 L2, float2 nR2, float2 G2
         at[1] = __fadd2_rn(at[1], e4);
         if constexpr (NP == kAllPowers) at[2] = __fadd2_rn(at[2], __fmul2_rn(e4, e4));
     } else if constexpr (NP == 0) {
-        const float2 xt = __fmul2_rn(x, G2);
+        const float2 xt = __ffma2_rn(v, GL2, nGR2);
         at[0] = __fadd2_rn(at[0], make_float2(ex2(xt.x), ex2(xt.y)));
     }
 }
@@ -172,7 +174,8 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
                                          float (&ct)[3], float &cy) {
     const float2 L2 = make_float2(kLog2e, kLog2e);
     const float2 nR2 = make_float2(-R, -R);
-    const float2 G2 = make_float2(g, g);
+    const float2 GL2 = make_float2(g * kLog2e, g * kLog2e);
+    const float2 nGR2 = make_float2(-g * R, -g * R);
     float2 a1[4], at[4][3], ay[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -189,7 +192,7 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
                 if constexpr (ENT && CLAMP) w[j] = max_nan_bf16x2(w[j], kFloorBf16x2);
                 const float2 v = make_float2(__uint_as_float(w[j] << 16),
                                              __uint_as_float(w[j] & 0xffff0000u));
-                step2<NP, ENT>(v, L2, nR2, G2, a1[j], at[j], ay[j]);
+                step2<NP, ENT>(v, L2, nR2, GL2, nGR2, a1[j], at[j], ay[j]);
             }
         } else {
             float f[4] = {__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
@@ -198,9 +201,9 @@ __device__ __forceinline__ void sum_vecs(const uint4 (&q)[VPL], float R, float g
 #pragma unroll
                 for (int j = 0; j < 4; ++j) f[j] = max_nan_f32(f[j], kFloorF32);
             }
-            step2<NP, ENT>(make_float2(f[0], f[1]), L2, nR2, G2, a1[(i & 1) * 2],
+            step2<NP, ENT>(make_float2(f[0], f[1]), L2, nR2, GL2, nGR2, a1[(i & 1) * 2],
                            at[(i & 1) * 2], ay[(i & 1) * 2]);
-            step2<NP, ENT>(make_float2(f[2], f[3]), L2, nR2, G2, a1[(i & 1) * 2 + 1],
+            step2<NP, ENT>(make_float2(f[2], f[3]), L2, nR2, GL2, nGR2, a1[(i & 1) * 2 + 1],
                            at[(i & 1) * 2 + 1], ay[(i & 1) * 2 + 1]);
         }
     }
