@@ -296,7 +296,7 @@ def walk(layout, logA: np.ndarray, u: np.ndarray, max_steps: int) -> dict:
     """MH transitions over each chain's subtree (section 3.2 step (3), Example 5).
 
     From the root, at each node whose request was scored: one transition;
-    move to the acceptance child if u <= A (Algorithm 1 line 7), else to the
+    move to the acceptance child if u <= A (the accept test of Algorithm 1), else to the
     rejection child.  Stop at a leaf, at a node whose request was deferred, or
     after max_steps (= K - k) transitions.  The reached state is the segment
     of the last accepted proposal, or the root segment.

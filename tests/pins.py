@@ -192,7 +192,7 @@ def pin_example5(walk):
     name = {f"v{i}": i for i in range(5)}
     seg_of = {"x": 0, "y": 1, "z": 2}
     logA = np.array([np.nan, math.log(0.6), math.log(0.3)])
-    # u <= A accepts (Algorithm 1 line 7); choose u on the stated side
+    # u <= A accepts (the accept test of Algorithm 1); choose u on the stated side
     u = np.ones(3)
     for node, dec in g["decisions"].items():
         s = int(lay.req[name[node]])
