@@ -1,8 +1,8 @@
 """Benchmark: scoring one prefetched subtree batch (and walking it) on GB300.
 
-One step = the whole hot path over one subtree batch already resident in HBM:
-per-token log p0 / log q_tau of every row (ps_score_rows), suffix sums and
-log A per request (ps_assemble_subtree), and the walk (ps_walk_subtree).
+One step = the whole hot path over one subtree batch already resident in HBM,
+in one call (ps_score_walk_subtree): per-token log p0 / log q_tau of every
+row, suffix sums and log A per request, and the walk of every chain.
 
 Default workload: the long-context batch, the largest of the five
 configurations that a single GPU holds: Qwen3-like vocabulary V = 151936
@@ -47,8 +47,8 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes (read + write) per launch of the scoring kernel on the default
 # workload, from one ncu capture of this kernel code (identified by its hash).
-NCU_TRAFFIC = {"source_sha1": "726286a81d5ed43f45d983e626b4d6049846d235",
-               "bytes_per_launch": 29923933440 + 7622912, "config": 3}
+NCU_TRAFFIC = {"source_sha1": "21a55dca796eface156d2333d3a6d0dce4178be4",
+               "bytes_per_launch": 29924102400 + 7043840, "config": 3}
 GENERAL_TAU = 0.3                   # a temperature whose 1/tau is not 1, 2, 4 or 8
 
 
@@ -341,10 +341,10 @@ def sweep_leg(ps, dev, stream, steps: int, warmup: int, per_point: bool = False,
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 with torch.cuda.stream(stream):
                     for _ in range(warmup):
-                        d.score_rows(stream), d.assemble(stream), d.walk(stream)
+                        d.step(stream)
                     ev[0].record(stream)
                     for _ in range(steps):
-                        d.score_rows(stream), d.assemble(stream), d.walk(stream)
+                        d.step(stream)
                     ev[1].record(stream)
                     ev[2].record(stream)
                     for _ in range(steps):
@@ -441,9 +441,7 @@ def steady_state_leg(ps, w, d, dev, stream, steps: int, warmup: int) -> dict:
                           status=cst)
 
     def one():
-        d2.score_rows(stream)
-        d2.assemble(stream)
-        d2.walk(stream)
+        d2.step(stream)
         ps.ps_carry_state(d2.batch, io, stream)
 
     with torch.cuda.stream(stream):
@@ -467,7 +465,8 @@ def steady_state_leg(ps, w, d, dev, stream, steps: int, warmup: int) -> dict:
     units = lay.suffix_tokens()
     return {"ms_per_step": ms, "value": units / (ms / 1e3), "unit": UNIT,
             "rows_scored": lay2.n_rows, "max_abs_dlogA_vs_step": float(dla.max()),
-            "step": "score (requests' rows) + assemble (carried root values) + walk + carry"}
+            "step": "score (requests' rows), suffix sums with carried root values and walk "
+                    "in one call, then carry"}
 
 
 def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
@@ -563,9 +562,7 @@ def main():
     alg_bytes_k1 = rows * (w.V * w.elem_bytes + 4 + 16)   # logits + token in, lp0/lq out
 
     def step():
-        d.score_rows(stream)
-        d.assemble(stream)
-        d.walk(stream)
+        d.step(stream)                  # ps_score_walk_subtree: scoring, sums and walk
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -641,9 +638,9 @@ def main():
                      "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
-        "gpu_launches": 3 * args.steps,
-        "kernel_launches_per_step": {"score_rows_kernel": 1, "assemble_kernel": 1,
-                                     "walk_kernel": 1},
+        "gpu_launches": 2 * args.steps,
+        "kernel_launches_per_step": {"score_rows_kernel": 1,
+                                     "assemble_kernel (suffix sums, log A and the walk)": 1},
         # what the suffix sums, log A and the walk add to a step after scoring
         "after_scoring_us": (ms_per_step - k1_avg) * 1e3,
         "clocks": clocks.summary(),

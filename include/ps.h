@@ -181,10 +181,11 @@ typedef struct {
 } ps_score_out;
 
 /*
- * Bytes of device workspace ps_score_subtree needs for this batch (depends
- * only on n_rows).  The workspace is scratch: per-row results when lp0/lq are
- * not requested, partial sums of rows that are split across warps, and their
- * arrival counters.  Returns 0 if batch is NULL.
+ * Bytes of device workspace the scoring calls need for this batch (depends
+ * only on n_rows and n_chains).  The workspace is scratch: per-row results
+ * when lp0/lq are not requested, partial sums of rows that are split across
+ * warps, their arrival counters, and one arrival counter per chain for
+ * ps_score_walk_subtree.  Returns 0 if batch is NULL.
  */
 size_t ps_score_workspace_bytes(const ps_subtree_batch *batch);
 
@@ -373,12 +374,34 @@ typedef struct {
  * Walk every chain's subtree from its root (section 3.2 step (3); Example 5;
  * Algorithm 2 MHTransition).  At a node whose request was scored, one
  * transition: move to the acceptance child if log u <= log A (u <= A,
- * Algorithm 1 line 7), else to the rejection child.  Stop at a leaf, at a node
+ * the accept test of Algorithm 1), else to the rejection child.  Stop at a leaf, at a node
  * whose request was deferred, or after max_steps transitions.
  * log_accept   [n_seg] device float64, as written by ps_score_subtree.
  */
 ps_status ps_walk_subtree(const ps_tree *tree, const double *log_accept,
                           const ps_walk_out *out, void *cuda_stream);
+
+/*
+ * One whole round in one call: ps_score_subtree, then ps_walk_subtree
+ * (section 3.2 steps (2)-(3); Algorithm 2, PrefetchAndScore then
+ * MHTransition).  Outputs are those of the two calls, bit for bit; the suffix
+ * sums and the walk run in one kernel, in which the last block of each chain
+ * to write its log A walks that chain, so the round takes two kernel launches
+ * instead of three.
+ *
+ * batch, out   as for ps_score_subtree.
+ * tree, wout   as for ps_walk_subtree; tree->n_chains and tree->n_seg must
+ *              equal the batch's (else PS_ERR_INVALID_ARG); the walk reads
+ *              out->log_accept.
+ * workspace    device memory, 256-byte aligned, >= ps_score_workspace_bytes().
+ * Device status bits go to out->status (scoring, suffix sums) and
+ * wout->status (walk), as in the two calls.  A chain whose segment layout
+ * fails the device checks (PS_DEV_BAD_LAYOUT) is not walked: its walk
+ * outputs are left unwritten.
+ */
+ps_status ps_score_walk_subtree(const ps_subtree_batch *batch, const ps_tree *tree,
+                                const ps_score_out *out, const ps_walk_out *wout,
+                                void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
  * Full structural check of a batch and its tree in HOST memory (synchronous;

@@ -8,7 +8,8 @@ raises.
 
 Entry points (see include/ps.h for the contract):
     ps_score_workspace_bytes, ps_score_subtree, ps_score_rows,
-    ps_assemble_subtree, ps_walk_subtree, ps_carry_state, ps_validate_subtree,
+    ps_assemble_subtree, ps_walk_subtree, ps_score_walk_subtree, ps_carry_state,
+    ps_validate_subtree,
     ps_score_subtree_noalloc, ps_status_string, ps_version
 Convenience: ``make_batch``, ``make_score_out``, ``make_tree``,
 ``make_walk_out`` build the structs from tensors; ``DeviceSubtree`` holds a
@@ -112,6 +113,10 @@ def lib() -> ctypes.CDLL:
         L.ps_score_subtree_noalloc.restype = ctypes.c_int
         L.ps_walk_subtree.argtypes = [ctypes.POINTER(PsTree), _vp, ctypes.POINTER(PsWalkOut), _vp]
         L.ps_walk_subtree.restype = ctypes.c_int
+        L.ps_score_walk_subtree.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsTree),
+                                            ctypes.POINTER(PsScoreOut), ctypes.POINTER(PsWalkOut),
+                                            _vp, ctypes.c_size_t, _vp]
+        L.ps_score_walk_subtree.restype = ctypes.c_int
         L.ps_carry_state.argtypes = [ctypes.POINTER(PsSubtreeBatch), ctypes.POINTER(PsCarryIo),
                                      _vp]
         L.ps_carry_state.restype = ctypes.c_int
@@ -243,6 +248,19 @@ def ps_walk_subtree(tree: PsTree, log_accept: torch.Tensor, out: PsWalkOut, stre
                                _stream(stream, log_accept))
     if check and st != PS_OK:
         raise PsError(st, "ps_walk_subtree")
+    return st
+
+
+def ps_score_walk_subtree(batch: PsSubtreeBatch, tree: PsTree, out: PsScoreOut,
+                          wout: PsWalkOut, workspace: torch.Tensor, stream=None,
+                          check: bool = True) -> int:
+    """Score, sum and walk one batch in one call (see include/ps.h)."""
+    ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = lib().ps_score_walk_subtree(ctypes.byref(batch), ctypes.byref(tree), ctypes.byref(out),
+                                     ctypes.byref(wout), ws_ptr, ws_bytes,
+                                     _stream(stream, workspace))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_score_walk_subtree")
     return st
 
 
@@ -556,10 +574,16 @@ class DeviceSubtree:
     def walk(self, stream=None) -> None:
         ps_walk_subtree(self.tree, self.t["log_accept"], self.walk_out, stream)
 
-    def step(self, stream=None) -> None:
-        """One pass of the whole path: score, then walk."""
-        self.score(stream)
-        self.walk(stream)
+    def step(self, stream=None, fused: bool = True) -> None:
+        """One pass of the whole path: score, sum and walk in one call
+        (ps_score_walk_subtree), or with fused=False in two
+        (ps_score_subtree, then ps_walk_subtree)."""
+        if fused:
+            ps_score_walk_subtree(self.batch, self.tree, self.score_out, self.walk_out,
+                                  self.workspace, stream)
+        else:
+            self.score(stream)
+            self.walk(stream)
 
     def carry(self, prev: dict | None = None, stream=None) -> dict:
         """Per-position values of each chain's reached state for the next

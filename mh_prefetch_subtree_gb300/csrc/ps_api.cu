@@ -15,20 +15,27 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace: per-row values (when the caller does not ask for them), the
+// split-row partials, then the per-chain arrival counters of the fused
+// suffix-sum + walk kernel directly followed by the row kernel's arrival
+// counters, so that one memset clears both.
 struct WsLayout {
     size_t rows_off, rows_bytes;
     size_t parts_off, parts_bytes;
+    size_t chain_cnt_off, chain_cnt_bytes;
     size_t cnt_off, cnt_bytes;
     size_t total;
 };
 
-WsLayout ws_layout(int64_t n_rows) {
+WsLayout ws_layout(int64_t n_rows, int32_t n_chains) {
     WsLayout w;
     w.rows_off = 0;
     w.rows_bytes = align_up((size_t)(n_rows > 0 ? n_rows : 0) * 2 * sizeof(double), kAlign);
     w.parts_off = w.rows_off + w.rows_bytes;
     w.parts_bytes = align_up((size_t)2 * ps::kMaxWarps * sizeof(ps::RowPart), kAlign);
-    w.cnt_off = w.parts_off + w.parts_bytes;
+    w.chain_cnt_off = w.parts_off + w.parts_bytes;
+    w.chain_cnt_bytes = align_up((size_t)(n_chains > 0 ? n_chains : 0) * sizeof(int32_t), kAlign);
+    w.cnt_off = w.chain_cnt_off + w.chain_cnt_bytes;
     w.cnt_bytes = align_up((size_t)ps::kMaxWarps * sizeof(int32_t), kAlign);
     w.total = w.cnt_off + w.cnt_bytes;
     return w;
@@ -125,7 +132,7 @@ const char *ps_status_string(ps_status s) {
 
 size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
     if (!batch) return 0;
-    return ws_layout(batch->n_rows).total;
+    return ws_layout(batch->n_rows, batch->n_chains).total;
 }
 
 }  // extern "C"
@@ -134,10 +141,13 @@ namespace {
 
 // Where the row kernel keeps its scratch: the split-row partials, the arrival
 // counters, and how many warps (one partial pair and one counter each) fit.
+// The memset before the launch clears [zero_from, counters + warps), so that
+// counters placed just before the row kernel's are cleared with them.
 struct RowsScratch {
     ps::RowPart *parts;
     int32_t *counters;
     int64_t max_warps;
+    int32_t *zero_from;
 };
 
 // Launch of the row kernel shared by every scoring entry point.  npow/g select
@@ -180,8 +190,8 @@ ps_status launch_rows(const ps_subtree_batch *b, int sms, const RowsScratch &scr
     p.status = status;
     const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
     // the counters must start at zero whatever the scratch held before
-    ps_status st =
-        map_cuda(cudaMemsetAsync(p.counters, 0, (size_t)warps * sizeof(int32_t), stream));
+    const size_t zero_bytes = (size_t)((uint8_t *)(p.counters + warps) - (uint8_t *)scr.zero_from);
+    ps_status st = map_cuda(cudaMemsetAsync(scr.zero_from, 0, zero_bytes, stream));
     if (st != PS_OK) return st;
     return map_cuda(ps::launch_score_rows(p, n_ctas, stream));
 }
@@ -191,7 +201,7 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
                             double *entropy, int32_t *status, void *workspace,
                             size_t workspace_bytes, void *cuda_stream, int32_t npow, float g,
                             const int32_t *tau_pow, int32_t n_taus, double *lq_multi) {
-    const WsLayout wl = ws_layout(b->n_rows);
+    const WsLayout wl = ws_layout(b->n_rows, b->n_chains);
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
         return PS_ERR_WORKSPACE;
     if (b->n_rows == 0) return PS_OK;
@@ -199,8 +209,8 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
     ps_status st = device_of(b->logits, &sms);
     if (st != PS_OK) return st;
     uint8_t *ws = (uint8_t *)workspace;
-    const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), (int32_t *)(ws + wl.cnt_off),
-                          ps::kMaxWarps};
+    int32_t *cnt = (int32_t *)(ws + wl.cnt_off);
+    const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxWarps, cnt};
     return launch_rows(b, sms, scr, lp0, lq, entropy, status, cuda_stream, npow, g, tau_pow,
                        n_taus, lq_multi);
 }
@@ -239,8 +249,13 @@ ps_status ps_score_rows_multi(const ps_subtree_batch *b, const double *taus, int
                              cuda_stream, top == 8 ? 16 : 17, 1.f, pw, n_taus, lq);
 }
 
-ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, const double *lq,
-                              const ps_score_out *out, void *cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks of ps_assemble_subtree's arguments.
+ps_status check_assemble_host(const ps_subtree_batch *b, const double *lp0, const double *lq,
+                              const ps_score_out *out) {
     if (!b || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0 ||
         !isfinite(b->alpha))
         return PS_ERR_INVALID_ARG;
@@ -249,10 +264,12 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     if (b->n_rows > 0 && (!lp0 || !lq)) return PS_ERR_INVALID_ARG;
     if ((b->root_lp0 == nullptr) != (b->root_lq == nullptr)) return PS_ERR_INVALID_ARG;
     if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
-    int sms = 0;
-    ps_status st = device_of(out->log_accept, &sms);
-    if (st != PS_OK) return st;
-    ps::AssembleParams a;
+    return PS_OK;
+}
+
+ps::AssembleParams assemble_params(const ps_subtree_batch *b, const double *lp0,
+                                   const double *lq, const ps_score_out *out) {
+    ps::AssembleParams a{};
     a.T = b->T;
     a.n_chains = b->n_chains;
     a.n_seg = b->n_seg;
@@ -275,29 +292,11 @@ ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, cons
     a.eps = b->eps;
     a.eps_class = out->eps_class;
     a.status = out->status;
-    return map_cuda(ps::launch_assemble(a, (cudaStream_t)cuda_stream));
+    return a;
 }
 
-ps_status ps_score_subtree(const ps_subtree_batch *b, const ps_score_out *out, void *workspace,
-                           size_t workspace_bytes, void *cuda_stream) {
-    ps_status st = check_batch_host(b);
-    if (st != PS_OK) return st;
-    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
-    const WsLayout wl = ws_layout(b->n_rows);
-    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
-        return PS_ERR_WORKSPACE;
-    uint8_t *ws = (uint8_t *)workspace;
-    double *lp0 = out->lp0 ? out->lp0 : (double *)(ws + wl.rows_off);
-    double *lq = out->lq ? out->lq : (double *)(ws + wl.rows_off) + b->n_rows;
-    if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
-    st = ps_score_rows(b, lp0, lq, out->entropy, out->status, workspace, workspace_bytes,
-                       cuda_stream);
-    if (st != PS_OK) return st;
-    return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
-}
-
-ps_status ps_walk_subtree(const ps_tree *t, const double *log_accept, const ps_walk_out *out,
-                          void *cuda_stream) {
+// Host checks of ps_walk_subtree's arguments.
+ps_status check_walk_host(const ps_tree *t, const double *log_accept, const ps_walk_out *out) {
     if (!t || !log_accept || !out) return PS_ERR_INVALID_ARG;
     if (t->n_chains < 1 || t->n_nodes < t->n_chains || t->n_seg < t->n_chains ||
         t->max_steps < 0)
@@ -306,10 +305,11 @@ ps_status ps_walk_subtree(const ps_tree *t, const double *log_accept, const ps_w
         return PS_ERR_INVALID_ARG;
     if (!out->state_seg || !out->end_node || !out->k_delta || !out->status)
         return PS_ERR_INVALID_ARG;
-    int sms = 0;
-    ps_status st = device_of(log_accept, &sms);
-    if (st != PS_OK) return st;
-    ps::WalkParams p;
+    return PS_OK;
+}
+
+ps::WalkParams walk_params(const ps_tree *t, const double *log_accept, const ps_walk_out *out) {
+    ps::WalkParams p{};
     p.n_chains = t->n_chains;
     p.n_nodes = t->n_nodes;
     p.n_seg = t->n_seg;
@@ -326,7 +326,89 @@ ps_status ps_walk_subtree(const ps_tree *t, const double *log_accept, const ps_w
     p.k_delta = out->k_delta;
     p.path = out->path;
     p.status = out->status;
-    return map_cuda(ps::launch_walk(p, (cudaStream_t)cuda_stream));
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+ps_status ps_assemble_subtree(const ps_subtree_batch *b, const double *lp0, const double *lq,
+                              const ps_score_out *out, void *cuda_stream) {
+    ps_status st = check_assemble_host(b, lp0, lq, out);
+    if (st != PS_OK) return st;
+    int sms = 0;
+    st = device_of(out->log_accept, &sms);
+    if (st != PS_OK) return st;
+    return map_cuda(ps::launch_assemble(assemble_params(b, lp0, lq, out),
+                                        (cudaStream_t)cuda_stream));
+}
+
+ps_status ps_score_subtree(const ps_subtree_batch *b, const ps_score_out *out, void *workspace,
+                           size_t workspace_bytes, void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(b->n_rows, b->n_chains);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
+        return PS_ERR_WORKSPACE;
+    uint8_t *ws = (uint8_t *)workspace;
+    double *lp0 = out->lp0 ? out->lp0 : (double *)(ws + wl.rows_off);
+    double *lq = out->lq ? out->lq : (double *)(ws + wl.rows_off) + b->n_rows;
+    if (out->eps_class && !(b->eps > 0.0 && b->eps < 0.5)) return PS_ERR_INVALID_ARG;
+    st = ps_score_rows(b, lp0, lq, out->entropy, out->status, workspace, workspace_bytes,
+                       cuda_stream);
+    if (st != PS_OK) return st;
+    return ps_assemble_subtree(b, lp0, lq, out, cuda_stream);
+}
+
+ps_status ps_walk_subtree(const ps_tree *t, const double *log_accept, const ps_walk_out *out,
+                          void *cuda_stream) {
+    ps_status st = check_walk_host(t, log_accept, out);
+    if (st != PS_OK) return st;
+    int sms = 0;
+    st = device_of(log_accept, &sms);
+    if (st != PS_OK) return st;
+    return map_cuda(ps::launch_walk(walk_params(t, log_accept, out), (cudaStream_t)cuda_stream));
+}
+
+ps_status ps_score_walk_subtree(const ps_subtree_batch *b, const ps_tree *t,
+                                const ps_score_out *out, const ps_walk_out *wout,
+                                void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    ps_status st = check_batch_host(b);
+    if (st != PS_OK) return st;
+    if (!out || !out->log_accept || !out->status) return PS_ERR_INVALID_ARG;
+    st = check_walk_host(t, out->log_accept, wout);
+    if (st != PS_OK) return st;
+    if (t->n_chains != b->n_chains || t->n_seg != b->n_seg) return PS_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(b->n_rows, b->n_chains);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < wl.total)
+        return PS_ERR_WORKSPACE;
+    uint8_t *ws = (uint8_t *)workspace;
+    double *lp0 = out->lp0 ? out->lp0 : (double *)(ws + wl.rows_off);
+    double *lq = out->lq ? out->lq : (double *)(ws + wl.rows_off) + b->n_rows;
+    st = check_assemble_host(b, lp0, lq, out);
+    if (st != PS_OK) return st;
+    int sms = 0;
+    st = device_of(b->n_rows > 0 ? b->logits : out->log_accept, &sms);
+    if (st != PS_OK) return st;
+    cudaStream_t stream = (cudaStream_t)cuda_stream;
+    int32_t *chain_cnt = (int32_t *)(ws + wl.chain_cnt_off);
+    int32_t *cnt = (int32_t *)(ws + wl.cnt_off);
+    if (b->n_rows > 0) {
+        // one memset clears the chain counters and the row kernel's counters
+        const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxWarps, chain_cnt};
+        st = launch_rows(b, sms, scr, lp0, lq, out->entropy, out->status, cuda_stream,
+                         integer_power(b->tau), (float)(1.0 / b->tau), nullptr, 0, nullptr);
+    } else {
+        st = map_cuda(cudaMemsetAsync(chain_cnt, 0, wl.chain_cnt_bytes, stream));
+    }
+    if (st != PS_OK) return st;
+    // right after the row kernel launched above, the suffix-sum kernel may read
+    // the layout before that kernel's results are visible (early)
+    return map_cuda(ps::launch_assemble_walk(assemble_params(b, lp0, lq, out),
+                                             walk_params(t, out->log_accept, wout), chain_cnt,
+                                             b->n_rows > 0, stream));
 }
 
 ps_status ps_validate_subtree(const ps_subtree_batch *b, const ps_tree *t, char *msg,
@@ -514,9 +596,9 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     double *lp0 = lp0_scratch ? (double *)base : out->lp0;
     double *lq = lq_scratch ? (double *)base + kNoAllocMaxRows : out->lq;
     if (b->n_rows > 0) {
-        const RowsScratch scr{(ps::RowPart *)(base + kNoAllocRowBytes),
-                              (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes),
-                              kNoAllocMaxWarps};
+        int32_t *cnt = (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes);
+        const RowsScratch scr{(ps::RowPart *)(base + kNoAllocRowBytes), cnt, kNoAllocMaxWarps,
+                              cnt};
         st = launch_rows(b, sms, scr, lp0, lq, out->entropy, out->status, cuda_stream,
                          integer_power(b->tau), (float)(1.0 / b->tau), nullptr, 0, nullptr);
         if (st != PS_OK) return st;

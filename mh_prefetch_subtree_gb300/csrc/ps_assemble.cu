@@ -13,21 +13,28 @@
 //
 // One CTA per segment (a chain root only writes NaN to its own entries).  It
 // is launched with programmatic dependent launch, so its CTAs may start while
-// the previous kernel finishes; every load of an input comes after
-// griddepcontrol.wait, which makes all of that kernel's writes visible.  The
-// threads stride over the rows in float64 and the block reduces in a fixed
-// order (warp butterfly, then warps in index order), so results are
-// bit-reproducible.  Every index is checked before use; a failing request
-// gets NaN outputs and a status bit.
+// the previous kernel finishes; griddepcontrol.wait makes all of that
+// kernel's writes visible before they are read.  The threads stride over the
+// rows in float64 and the block reduces in a fixed order (warp butterfly, then
+// warps in index order), so results are bit-reproducible.  Every index is
+// checked before use; a failing request gets NaN outputs and a status bit.
+//
+// The fused form, used when one call scores, sums and walks, also takes the
+// walk (section 3.2 step (3)): the last CTA of each chain to write its log A
+// walks the chain, so the round needs no third launch.
 #include <math.h>
 
-#include "ps_internal.cuh"
+#include <type_traits>
+
+#include "ps_walk_chain.cuh"
 
 namespace ps {
 namespace {
 
+// 256 threads per segment: wider blocks measured slower (1024 threads took
+// 17 us instead of 11 on the long-context batch), since they hold fewer loads
+// in flight per thread and wait longer at the block reduction.
 constexpr int kAssembleThreads = 256;
-constexpr int kAssembleWarps = kAssembleThreads / 32;
 
 __device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
@@ -94,18 +101,29 @@ __device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
     return lo;
 }
 
-__global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const AssembleParams p) {
-    __shared__ double red[4][kAssembleWarps];
+// One block per segment.  FUSED: the last CTA of each
+// chain to finish (arrivals counted in chain_cnt, zeroed before the launch)
+// also walks that chain with its first warp, so that the walk needs no launch
+// of its own.  EARLY: the kernel directly follows libps's own scoring kernel,
+// launched in the same call, so the caller's inputs were written before that
+// kernel started and the metadata may be loaded before griddepcontrol.wait;
+// only the per-row values wait.  Without EARLY nothing is read before the
+// wait, because the previous kernel may be the caller's own kernel writing
+// the layout arrays.
+template <bool FUSED, bool EARLY>
+__global__ void __launch_bounds__(kAssembleThreads)
+    assemble_kernel(const AssembleParams p, const WalkParams wp, int32_t *chain_cnt) {
+    constexpr int kWarps = kAssembleThreads / 32;
+    __shared__ double red[4][kWarps];
+    __shared__ typename std::conditional<FUSED, WalkSmem, int>::type wsm;
+    __shared__ int walk_here;
     const int32_t s = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const double qnan = __longlong_as_double(0x7ff8000000000000ll);
-    pdl_launch_dependents();                         // the walk may be scheduled now
-    // Wait for the previous kernel in the stream before reading anything: the
-    // per-row values come from the scoring kernel, and the caller may have
-    // written the layout arrays with a kernel just before this call.
-    pdl_wait_prerequisites();
+    pdl_launch_dependents();                         // the next kernel may be scheduled now
+    if constexpr (!EARLY) pdl_wait_prerequisites();
     const int c = chain_of(p.chain_seg0, p.n_chains, s);
     // metadata in two rounds of loads: what depends on s (and c) only, then
     // the root's and src's entries (indices clamped in range, checked below)
@@ -115,112 +133,131 @@ __global__ void __launch_bounds__(kAssembleThreads) assemble_kernel(const Assemb
     const int32_t src = p.seg_src[s];
     const int64_t y0 = p.seg_row0[s];
     const int64_t y1 = p.seg_row0[s + 1];
-    if (s == s0) {                                   // a chain root
-        if (tid == 0) {
-            double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
-            for (int j = 0; j < 6; ++j)
-                if (outs[j]) outs[j][s] = qnan;
-            if (p.eps_class) p.eps_class[s] = -1;
-        }
-        return;
-    }
+    const bool chain_ok = s0 >= 0 && s1 <= p.n_seg && s1 > s0 && s >= s0 && s < s1;
+    const bool root = chain_ok && s == s0;           // a chain root: NaN entries only
     const int32_t T = p.T;
-    int32_t bits = 0;
-    if (s0 < 0 || s1 > p.n_seg || s1 <= s0 || s < s0 || s >= s1) bits |= PS_DEV_BAD_LAYOUT;
-    const int32_t s0l = bits ? s : s0;
-    const bool src_root = src == s0;
-    const bool src_ok = src_root || (src > s0 && src < s1 && src != s);
-    const int32_t srcl = (bits == 0 && src_ok) ? src : s;
-    const int32_t rc = p.seg_cut[s0l];
-    const int32_t rsrc = p.seg_src[s0l];
-    const int64_t r0 = p.seg_row0[s0l];
-    const int64_t r1 = p.seg_row0[s0l + 1];
-    const int32_t csrc_l = p.seg_cut[srcl];
-    const int64_t q0_l = p.seg_row0[srcl];
-    const int64_t q1_l = p.seg_row0[srcl + 1];
-    if (bits == 0) {
-        if (rsrc != -1 || rc < 0 || rc > T || r0 < 0 || r1 > p.n_rows ||
-            r1 - r0 != (int64_t)(T - rc))
-            bits |= PS_DEV_BAD_LAYOUT;
-        if (cs < 0 || cs > T - 1 || y0 < 0 || y1 > p.n_rows || y1 - y0 != (int64_t)(T - cs))
-            bits |= PS_DEV_BAD_LAYOUT;
-        if (!src_ok) bits |= PS_DEV_BAD_LAYOUT;
-    }
-    int32_t csrc = T;
-    int64_t q0 = 0, q1 = 0;
-    if (bits == 0 && !src_root) {
-        csrc = csrc_l;
-        q0 = q0_l;
-        q1 = q1_l;
-        if (csrc < 0 || csrc > T - 1 || q0 < 0 || q1 > p.n_rows ||
-            q1 - q0 != (int64_t)(T - csrc))
-            bits |= PS_DEV_BAD_LAYOUT;
-    }
-    // Condition 1; and without carried root values, the root rows must cover
-    // every position a request's x suffix reads
-    if (bits == 0 && (cs > csrc || (cs < rc && p.root_lp0 == nullptr))) bits |= PS_DEV_INFEASIBLE;
-
+    int32_t bits = chain_ok ? 0 : PS_DEV_BAD_LAYOUT;
     double ly = qnan, qy = qnan, lx = qnan, qx = qnan;
-    if (bits == 0) {                                 // uniform across the block
-        double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
-        // y: the request's own rows.  x: positions cs+1..csrc of the current
-        // state (carried values up to the root's cut, root rows above it),
-        // then all rows of src
-        const int32_t k1 = min(rc, csrc);               // last carried position
-        const int32_t lo = max(cs, rc);                 // rows cover positions > rc
-        Ranges g;
-        g.lp[0] = p.lp0, g.lq[0] = p.lq, g.o[0] = y0, g.n[0] = y1 - y0;
-        g.lp[1] = p.root_lp0, g.lq[1] = p.root_lq, g.o[1] = (int64_t)c * T + cs;
-        g.n[1] = cs < k1 ? (int64_t)(k1 - cs) : 0;
-        g.lp[2] = p.lp0, g.lq[2] = p.lq, g.o[2] = r0 + (lo - rc);
-        g.n[2] = lo < csrc ? (int64_t)(csrc - lo) : 0;
-        g.lp[3] = p.lp0, g.lq[3] = p.lq, g.o[3] = q0, g.n[3] = q1 - q0;
-        ranges_sum(g, tid, a, b, e, f);
-        a = warp_sum(a);
-        b = warp_sum(b);
-        e = warp_sum(e);
-        f = warp_sum(f);
-        if (lane == 0) {
-            red[0][warp] = a;
-            red[1][warp] = b;
-            red[2][warp] = e;
-            red[3][warp] = f;
+    if (!root) {
+        const int32_t s0l = bits ? s : s0;
+        const bool src_root = src == s0;
+        const bool src_ok = src_root || (src > s0 && src < s1 && src != s);
+        const int32_t srcl = (bits == 0 && src_ok) ? src : s;
+        const int32_t rc = p.seg_cut[s0l];
+        const int32_t rsrc = p.seg_src[s0l];
+        const int64_t r0 = p.seg_row0[s0l];
+        const int64_t r1 = p.seg_row0[s0l + 1];
+        const int32_t csrc_l = p.seg_cut[srcl];
+        const int64_t q0_l = p.seg_row0[srcl];
+        const int64_t q1_l = p.seg_row0[srcl + 1];
+        if (bits == 0) {
+            if (rsrc != -1 || rc < 0 || rc > T || r0 < 0 || r1 > p.n_rows ||
+                r1 - r0 != (int64_t)(T - rc))
+                bits |= PS_DEV_BAD_LAYOUT;
+            if (cs < 0 || cs > T - 1 || y0 < 0 || y1 > p.n_rows || y1 - y0 != (int64_t)(T - cs))
+                bits |= PS_DEV_BAD_LAYOUT;
+            if (!src_ok) bits |= PS_DEV_BAD_LAYOUT;
         }
-        __syncthreads();
-        if (tid == 0) {
-            ly = qy = lx = qx = 0.0;
-            for (int w = 0; w < kAssembleWarps; ++w) {
-                ly += red[0][w];
-                qy += red[1][w];
-                lx += red[2][w];
-                qx += red[3][w];
+        int32_t csrc = T;
+        int64_t q0 = 0, q1 = 0;
+        if (bits == 0 && !src_root) {
+            csrc = csrc_l;
+            q0 = q0_l;
+            q1 = q1_l;
+            if (csrc < 0 || csrc > T - 1 || q0 < 0 || q1 > p.n_rows ||
+                q1 - q0 != (int64_t)(T - csrc))
+                bits |= PS_DEV_BAD_LAYOUT;
+        }
+        // Condition 1; and without carried root values, the root rows must
+        // cover every position a request's x suffix reads
+        if (bits == 0 && (cs > csrc || (cs < rc && p.root_lp0 == nullptr)))
+            bits |= PS_DEV_INFEASIBLE;
+
+        if constexpr (EARLY) pdl_wait_prerequisites();   // per-row values are now visible
+        if (bits == 0) {                                 // uniform across the block
+            double a = 0.0, b = 0.0, e = 0.0, f = 0.0;
+            // y: the request's own rows.  x: positions cs+1..csrc of the current
+            // state (carried values up to the root's cut, root rows above it),
+            // then all rows of src
+            const int32_t k1 = min(rc, csrc);               // last carried position
+            const int32_t lo = max(cs, rc);                 // rows cover positions > rc
+            Ranges g;
+            g.lp[0] = p.lp0, g.lq[0] = p.lq, g.o[0] = y0, g.n[0] = y1 - y0;
+            g.lp[1] = p.root_lp0, g.lq[1] = p.root_lq, g.o[1] = (int64_t)c * T + cs;
+            g.n[1] = cs < k1 ? (int64_t)(k1 - cs) : 0;
+            g.lp[2] = p.lp0, g.lq[2] = p.lq, g.o[2] = r0 + (lo - rc);
+            g.n[2] = lo < csrc ? (int64_t)(csrc - lo) : 0;
+            g.lp[3] = p.lp0, g.lq[3] = p.lq, g.o[3] = q0, g.n[3] = q1 - q0;
+            ranges_sum(g, tid, a, b, e, f);
+            a = warp_sum(a);
+            b = warp_sum(b);
+            e = warp_sum(e);
+            f = warp_sum(f);
+            if (lane == 0) {
+                red[0][warp] = a;
+                red[1][warp] = b;
+                red[2][warp] = e;
+                red[3][warp] = f;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                ly = qy = lx = qx = 0.0;
+                for (int w = 0; w < kWarps; ++w) {
+                    ly += red[0][w];
+                    qy += red[1][w];
+                    lx += red[2][w];
+                    qx += red[3][w];
+                }
             }
         }
     }
     if (tid == 0) {
         if (bits) set_status(p.status, bits);
-        const double r = (qx - qy) + p.alpha * (ly - lx);
-        const double la = (r != r) ? qnan : fmin(0.0, r);
-        if (p.lp_y) p.lp_y[s] = ly;
-        if (p.lq_y) p.lq_y[s] = qy;
-        if (p.lp_x) p.lp_x[s] = lx;
-        if (p.lq_x) p.lq_x[s] = qx;
-        if (p.log_ratio) p.log_ratio[s] = r;
-        p.log_accept[s] = la;
-        if (p.eps_class) {
-            // epsilon-certainty (section 3.3), compared in the log domain:
-            // A <= eps  <=>  log A <= log eps;  A >= 1 - eps  <=>  log A >= log1p(-eps)
-            int8_t cls = -1;
-            if (la == la) cls = la <= log(p.eps) ? 0 : (la >= log1p(-p.eps) ? 2 : 1);
-            p.eps_class[s] = cls;
+        if (root) {
+            double *outs[6] = {p.lp_y, p.lq_y, p.lp_x, p.lq_x, p.log_ratio, p.log_accept};
+            for (int j = 0; j < 6; ++j)
+                if (outs[j]) outs[j][s] = qnan;
+            if (p.eps_class) p.eps_class[s] = -1;
+        } else {
+            const double r = (qx - qy) + p.alpha * (ly - lx);
+            const double la = (r != r) ? qnan : fmin(0.0, r);
+            if (p.lp_y) p.lp_y[s] = ly;
+            if (p.lq_y) p.lq_y[s] = qy;
+            if (p.lp_x) p.lp_x[s] = lx;
+            if (p.lq_x) p.lq_x[s] = qx;
+            if (p.log_ratio) p.log_ratio[s] = r;
+            p.log_accept[s] = la;
+            if (p.eps_class) {
+                // epsilon-certainty (section 3.3), compared in the log domain:
+                // A <= eps  <=>  log A <= log eps;  A >= 1 - eps  <=>  log A >= log1p(-eps)
+                int8_t cls = -1;
+                if (la == la) cls = la <= log(p.eps) ? 0 : (la >= log1p(-p.eps) ? 2 : 1);
+                p.eps_class[s] = cls;
+            }
+        }
+    }
+    if constexpr (FUSED) {
+        // the last CTA of the chain to get here walks it (a chain whose layout
+        // failed the checks above is not walked; its status bit is set)
+        if (tid == 0) {
+            int last = 0;
+            if (chain_ok) {
+                __threadfence();                      // this CTA's log A before its arrival
+                last = atomicAdd(chain_cnt + c, 1) == s1 - s0 - 1;
+            }
+            walk_here = last;
+        }
+        __syncthreads();
+        if (walk_here) {
+            __threadfence();                          // every arrival's log A is visible
+            if (warp == 0) walk_chain(wp, c, wsm, lane);
         }
     }
 }
 
-}  // namespace
-
-cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream) {
-    if (p.n_seg <= 0 || p.n_chains <= 0) return cudaSuccess;
+template <bool FUSED, bool EARLY>
+cudaError_t launch_t(const AssembleParams &p, const WalkParams &wp, int32_t *chain_cnt,
+                     cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_seg);
     cfg.blockDim = dim3(kAssembleThreads);
@@ -231,7 +268,22 @@ cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, assemble_kernel, p);
+    return cudaLaunchKernelEx(&cfg, assemble_kernel<FUSED, EARLY>, p, wp, chain_cnt);
+}
+
+}  // namespace
+
+cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream) {
+    if (p.n_seg <= 0 || p.n_chains <= 0) return cudaSuccess;
+    const WalkParams none{};
+    return launch_t<false, false>(p, none, nullptr, stream);
+}
+
+cudaError_t launch_assemble_walk(const AssembleParams &p, const WalkParams &wp,
+                                 int32_t *chain_cnt, bool early, cudaStream_t stream) {
+    if (p.n_seg <= 0 || p.n_chains <= 0) return cudaSuccess;
+    return early ? launch_t<true, true>(p, wp, chain_cnt, stream)
+                 : launch_t<true, false>(p, wp, chain_cnt, stream);
 }
 
 }  // namespace ps

@@ -115,6 +115,12 @@ struct WalkParams {
 // predecessor may be the caller's own kernel writing those inputs.
 cudaError_t launch_score_rows(const RowsParams &p, int n_ctas, cudaStream_t stream);
 cudaError_t launch_assemble(const AssembleParams &p, cudaStream_t stream);
+// Suffix sums and log A, then each chain's walk by the last CTA of the chain to
+// finish; chain_cnt [n_chains] must be zero at launch.  early: the previous
+// kernel in the stream is libps's own scoring kernel of the same call, so the
+// layout arrays may be read before griddepcontrol.wait.
+cudaError_t launch_assemble_walk(const AssembleParams &p, const WalkParams &wp,
+                                 int32_t *chain_cnt, bool early, cudaStream_t stream);
 cudaError_t launch_walk(const WalkParams &p, cudaStream_t stream);
 cudaError_t launch_carry(const CarryParams &p, cudaStream_t stream);
 size_t score_rows_smem_bytes();
