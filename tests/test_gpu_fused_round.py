@@ -67,14 +67,14 @@ def test_one_call_round_equals_the_two_calls(case):
     elif case == "config2_small":
         w = make_workload(2, device=DEV, T=96, n_pf=10, seed=31)
     elif case == "many_chains":
-        w = _chains(300, 24, 6, seed=32)               # > 256 segments: 256-thread blocks
+        w = _chains(300, 24, 6, seed=32)               # 2,100 segments, many waves of blocks
     elif case == "empty_chains":
         w = _chains(12, 16, 4, seed=33, every_third_empty=True)
     elif case == "no_rows":
         w = _chains(5, 8, 0, seed=34)
     else:
-        # segments of up to 6000 rows: a request's sums take two rounds of
-        # loads even with 1024 threads
+        # segments of up to 6000 rows: a request's sums take several rounds of
+        # loads per thread
         w = _chains(1, 6000, 6, V=1024, seed=35)
     a = _run(w, fused=True)
     b = _run(w, fused=False)
@@ -89,9 +89,9 @@ def test_one_call_round_equals_the_two_calls(case):
 
 @pytest.mark.parametrize("tau", [0.25, 0.3])
 def test_masked_rows_among_ordinary_rows_in_the_entropy_variant(tau):
-    # without the masked-logits hint a warp switches to clamped sums at its
-    # first -inf; rows after that (masked or not, peaked or flat) must still
-    # match the oracle, and so must the rows of warps that never switch
+    # without the masked-logits hint, chunks holding a -inf take the clamped
+    # slow path while the other chunks of the same warps stay on the fast
+    # path; masked, flat and peaked rows side by side must all match the oracle
     V = 151936
     rng = np.random.default_rng(41)
     trees = [bfs_tree(rng, 40, 6) for _ in range(3)]
