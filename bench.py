@@ -469,6 +469,25 @@ def steady_state_leg(ps, w, d, dev, stream, steps: int, warmup: int) -> dict:
                     "in one call, then carry"}
 
 
+def graph_leg(d, stream, steps: int, units: int) -> dict:
+    """The same round captured once in a CUDA graph and replayed `steps` times:
+    what the step costs without the host-side work of each call (informative;
+    it matters for small batches, where that work is a large share)."""
+    with torch.cuda.stream(stream):
+        d.step(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        d.step(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    ms = kernel_loop(stream, steps, g.replay)
+    return {"ms_per_step": ms, "value": units / (ms / 1e3), "unit": UNIT,
+            "how": "ps_score_walk_subtree captured in one CUDA graph, replayed back to back"}
+
+
 def host_tree_timing(ps, T: int, n_pf: int, reps: int = 200) -> dict:
     """Host-side tree construction (ps_build_bfs_tree, ps_predictive_allocation)
     per call through the binding, for the bench's T and request budget.  The
@@ -523,6 +542,8 @@ def main():
                     help="leave the 36-point throughput sweep out of the bench line")
     ap.add_argument("--no-extras", action="store_true",
                     help="time only the step and the scoring kernel (for profiling runs)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the round captured in a CUDA graph and replayed")
     ap.add_argument("--sweep", action="store_true",
                     help="time the 36-point throughput sweep alone, one line per point")
     ap.add_argument("--sweep-steps", type=int, default=2)
@@ -602,6 +623,8 @@ def main():
         extras = variant_legs(ps, w, d, dev, stream, args.steps, logits_bytes)
         n_ch, T = lay.n_chains, lay.T
         extras["tree_construction"] = host_tree_timing(ps, T, int(w.info.get("n_requests", 16)))
+        if args.graph:
+            extras["graph_replay"] = graph_leg(d, stream, args.steps, units_per_step)
         if ws == 1 and getattr(w.layout, "trees", None):
             extras["steady_state"] = steady_state_leg(ps, w, d, dev, stream, args.steps,
                                                       args.warmup)
