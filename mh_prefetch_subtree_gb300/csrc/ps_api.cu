@@ -615,8 +615,8 @@ extern "C" ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status
     return map_cuda(ps::launch_wait_selftest(limit_ns, status, (cudaStream_t)cuda_stream));
 }
 
-ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
-                                    void *cuda_stream) {
+extern "C" ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
+                                      void *cuda_stream) {
     if (!b || !io || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)
         return PS_ERR_INVALID_ARG;
     if (!b->chain_seg0 || !b->seg_row0 || !b->seg_cut || !b->seg_src) return PS_ERR_INVALID_ARG;
