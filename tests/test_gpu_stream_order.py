@@ -7,7 +7,8 @@ kernel: here a torch kernel rewrites the uniforms, the tree arrays or the
 segment arrays immediately before the call, on the same stream, after a
 kernel that filled them with wrong values.  The results must be those of a
 run on inputs written long before (the walk and log A of the PreSTO round,
-section 3.2 step (3) and eq. (6)).
+section 3.2 step (3) and eq. (6)).  The same holds for ps_score_walk_subtree,
+whose suffix-sum + walk kernel reads the layout early.
 """
 
 import numpy as np
@@ -119,3 +120,44 @@ def test_segments_written_by_a_kernel_just_before_the_suffix_sums():
         assert torch.equal(la[req], ref.t["log_accept"][req]), it
         assert torch.equal(lr[req], ref.t["log_ratio"][req]), it
         assert bool(torch.isnan(la[~req]).all())
+
+
+def test_inputs_written_by_a_kernel_just_before_the_one_call_round():
+    # ps_score_walk_subtree launches its scoring kernel without early start, so
+    # that kernel sees the caller's writes; the suffix-sum + walk kernel reads
+    # the layout before waiting on the scoring kernel, which is only safe
+    # because the caller's kernels finished before the scoring kernel began
+    w = make_workload(2, device=DEV, T=64, n_pf=12, seed=93)
+    ref = _reference(w)
+    n_seg = int(ref.t["seg_cut"].shape[0])
+    good = torch.zeros(BIG, dtype=torch.int32, device=DEV)
+    good[:n_seg] = ref.t["seg_cut"]
+    good[n_seg:2 * n_seg] = ref.t["seg_src"]
+    bad = torch.zeros(BIG, dtype=torch.int32, device=DEV)
+    bad[:n_seg] = 1
+    bad[n_seg:2 * n_seg] = torch.roll(ref.t["seg_src"], 1)
+    buf = torch.empty(BIG, dtype=torch.int32, device=DEV)
+    ug = torch.zeros(BIG, dtype=torch.float64, device=DEV)
+    ug[:n_seg] = ref.t["u"]
+    ub = torch.full((BIG,), 1e-300, dtype=torch.float64, device=DEV)
+    u_buf = torch.empty(BIG, dtype=torch.float64, device=DEV)
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps)
+    d.batch.seg_cut, d.batch.seg_src = buf[:n_seg].data_ptr(), buf[n_seg:2 * n_seg].data_ptr()
+    d.tree.u = u_buf[:n_seg].data_ptr()
+    d.batch._keep = d.batch._keep + (buf,)
+    d.tree._keep = d.tree._keep + (u_buf,)
+    req = torch.from_numpy(~w.layout.is_root()).to(DEV)
+    for it in range(10):
+        for k in ("status", "wstatus"):
+            d.t[k].zero_()
+        d.t["log_accept"].fill_(7.0)
+        _rewrite(u_buf, ug, ub)
+        _rewrite(buf, good, bad)                # the kernel right before the call
+        d.step()
+        torch.cuda.synchronize()
+        st = int(d.t["status"].item()) | int(d.t["wstatus"].item())
+        assert st == 0, ps.dev_status_names(st)
+        assert torch.equal(d.t["log_accept"][req], ref.t["log_accept"][req]), it
+        for k in ("state_seg", "end_node", "k_delta", "path"):
+            assert torch.equal(d.t[k], ref.t[k]), (it, k)
