@@ -395,9 +395,10 @@ ps_status ps_walk_subtree(const ps_tree *tree, const double *log_accept,
  *              out->log_accept.
  * workspace    device memory, 256-byte aligned, >= ps_score_workspace_bytes().
  * Device status bits go to out->status (scoring, suffix sums) and
- * wout->status (walk), as in the two calls.  A chain whose segment layout
- * fails the device checks (PS_DEV_BAD_LAYOUT) is not walked: its walk
- * outputs are left unwritten.
+ * wout->status (walk), as in the two calls.  A chain whose chain_seg0
+ * bounds fail the device checks (PS_DEV_BAD_LAYOUT) is not walked: its walk
+ * outputs are left unwritten.  Other layout failures give the request NaN
+ * outputs, and the walk treats it as rejected.
  */
 ps_status ps_score_walk_subtree(const ps_subtree_batch *batch, const ps_tree *tree,
                                 const ps_score_out *out, const ps_walk_out *wout,

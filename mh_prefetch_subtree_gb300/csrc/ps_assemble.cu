@@ -237,8 +237,9 @@ __global__ void __launch_bounds__(kAssembleThreads)
         }
     }
     if constexpr (FUSED) {
-        // the last CTA of the chain to get here walks it (a chain whose layout
-        // failed the checks above is not walked; its status bit is set)
+        // the last CTA of the chain to get here walks it (a chain whose
+        // chain_seg0 bounds failed the checks above is not counted, so not
+        // walked; its status bit is set)
         if (tid == 0) {
             int last = 0;
             if (chain_ok) {
