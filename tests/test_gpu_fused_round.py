@@ -114,3 +114,34 @@ def test_masked_rows_among_ordinary_rows_in_the_entropy_variant(tau):
                  logits=x, tokens=tok, u=1.0 - rng.random(lay.n_seg), max_steps=100)
     s = H.full_parity(w)
     assert s["lp0_max_rel"] <= H.TOK_RTOL
+
+
+def test_one_call_round_with_invalid_chain_bounds():
+    # the last chain's end in chain_seg0 points past n_seg (a layout the host
+    # validator rejects, given to the device anyway): its requests get NaN and
+    # PS_DEV_BAD_LAYOUT, it is not walked (its outputs keep their old values),
+    # and the other chains are scored and walked as before
+    w = _chains(3, 16, 4, seed=36)
+    ref = _run(w, fused=True)
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps,
+                                entropy=True, eps=H.EPS)
+    d.t["chain_seg0"][-1] += 5
+    for k in ("state_seg", "end_node", "k_delta", "path"):
+        d.t[k].fill_(-7)
+    d.step()
+    torch.cuda.synchronize()
+    assert int(d.t["status"].item()) & 0x10
+    lay = w.layout
+    s2 = int(lay.chain_seg0[2])
+    la = d.t["log_accept"].cpu().numpy()
+    assert np.isnan(la[s2:]).all()
+    assert np.array_equal(la[:s2], ref["log_accept"][:s2], equal_nan=True)
+    stride = w.max_steps + 1
+    for k in ("state_seg", "end_node", "k_delta"):
+        got = d.t[k].cpu().numpy()
+        assert np.array_equal(got[:2], ref[k][:2]), k
+        assert got[2] == -7, k
+    path = d.t["path"].cpu().numpy()
+    assert np.array_equal(path[:2 * stride], ref["path"][:2 * stride])
+    assert (path[2 * stride:] == -7).all()
