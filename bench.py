@@ -185,6 +185,18 @@ def build_workload(config: int, dev, rank: int, n_pf=None):
     return make_workload(config, device=dev, **kw)
 
 
+def host_memory_available() -> int | None:
+    """MemAvailable of /proc/meminfo in bytes, or None where it cannot be read."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def cpu_model() -> str:
     """The host CPU's model name (lscpu), for the baseline's record."""
     try:
@@ -633,7 +645,17 @@ def main():
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_leg(ps, w, d, dev, stream, args, ws)
+        # every rank on this host pins its own copy of the batch's inputs; if
+        # the host cannot hold them all, no rank runs the leg (it has barriers)
+        need = logits_bytes + rows * 4 + (1 << 30)
+        local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(ws)))
+        avail = host_memory_available()
+        short = 1.0 if avail is not None and avail < local_ranks * need * 1.25 + (8 << 30) else 0.0
+        if max_over_ranks(short, dev) > 0:
+            e2e = {"skipped": f"pinning {local_ranks} x {need / 1e9:.1f} GB of inputs would "
+                              f"exceed the host's available memory ({(avail or 0) / 1e9:.0f} GB)"}
+        else:
+            e2e = e2e_leg(ps, w, d, dev, stream, args, ws)
 
     peak, peak_src = peaks()
     achieved = alg_bytes_k1 / (k1_avg / 1e3) / 1e9

@@ -39,7 +39,17 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile what is stale and link libps.so.  Processes that build at the
+    same time (one per rank under torchrun, say) take turns on a lock file, so
+    no two of them write the same object file."""
+    import fcntl
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, verbose)
+
+
+def _build_locked(force: bool, verbose: bool) -> str:
     headers = [os.path.join(CSRC, "ps_internal.cuh"), os.path.join(ROOT, "include", "ps.h")]
     procs, objs = [], []
     for src in SOURCES:
