@@ -666,11 +666,14 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        # the arithmetic: float32 exponent sums per row, float64 per-row finish
+        # and suffix sums; the logits themselves are stored as config.logits_dtype
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded logits, trees of the configuration's rule, proposal tokens "
                 "drawn from q_tau)",
         "config": {"workload": w.name, "V": w.V, "T": lay.T, "n_requests": lay.n_seg - lay.n_chains,
                    "rows": rows, "suffix_tokens": units_per_step, "logits_bytes": logits_bytes,
+                   "logits_dtype": w.dtype,
                    "alpha": w.alpha, "tau": w.tau,
                    "l2": f"inputs {logits_bytes / 1e9:.1f} GB > 129 MB L2; no flush",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
