@@ -225,8 +225,9 @@ def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
     t1 = time.time()
     sums = oracle.suffix_sums(lay, lp0, lq)
     _, la = oracle.log_accept(sums, w.alpha)
-    oracle.walk(lay, la, w.u, w.max_steps)
+    wk = oracle.walk(lay, la, w.u, w.max_steps)
     t2 = time.time()
+    ref = dict(lp0=lp0, lq=lq, log_accept=la, walk=wk)
     dt = t2 - t0
     # one core: time growing row samples until one takes over max_seconds / 6
     n1, tr1 = 64, 0.0
@@ -238,13 +239,44 @@ def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
             break
         n1 = min(w.n_rows, n1 * 4)
     one_core_s = tr1 * w.n_rows / n1 + (t2 - t1)
-    return {"value": units / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+    return ref, {"value": units / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "cpu": cpu_model(), "nproc": os.cpu_count(),
             "sample": f"the whole batch ({w.n_rows} rows, {units} suffix tokens), "
                       f"{dt:.1f} s wall on {threads} threads",
             "one_core": {"value": units / one_core_s, "unit": UNIT, "cores": 1,
                          "sample": f"per-row part timed on {n1} rows ({tr1:.1f} s) and "
                                    f"scaled to {w.n_rows}; sums and walk as measured"}}
+
+
+def parity_vs_oracle(w, d, ref) -> dict:
+    """The timed batch's GPU results against the oracle's on the same bytes:
+    worst per-token relative errors, worst log A error, and walks compared
+    chain by chain (a walk may differ only after a decision whose log u lies
+    within 1e-3 of log A, a near-tie)."""
+    lay = w.layout
+    req = ~lay.is_root()
+    out = {}
+    for k in ("lp0", "lq"):
+        g, o = d.t[k].cpu().numpy(), ref[k]
+        m = np.isfinite(o)
+        out[f"{k}_max_rel"] = float(np.max(np.abs(g[m] - o[m]) / np.maximum(np.abs(o[m]), 1e-300)))
+    la_g = d.t["log_accept"].cpu().numpy()
+    out["log_accept_max_abs"] = float(np.max(np.abs(la_g[req] - ref["log_accept"][req])))
+    wk = ref["walk"]
+    state, kd = d.t["state_seg"].cpu().numpy(), d.t["k_delta"].cpu().numpy()
+    differ = int(np.sum((state != wk["state_seg"]) | (kd != wk["k_delta"])))
+    ties = 0
+    for c in range(lay.n_chains):
+        for v in wk["path"][c][:-1]:
+            s = int(lay.req[v])
+            if s >= 0 and abs(np.log(w.u[s]) - ref["log_accept"][s]) < 1e-3:
+                ties += 1
+    import oracle
+    out.update({"walks_differing": differ, "near_ties_on_oracle_paths": ties,
+                "eps_certain": oracle.eps_certain_fraction(ref["log_accept"][req]),
+                "tolerances": "per token 1e-4 relative, log A 1e-3 absolute",
+                "checked": f"all {lay.n_rows} rows and {int(req.sum())} requests of the batch"})
+    return out
 
 
 def reference_arm(args, ws, rank):
@@ -697,7 +729,8 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        ref, line["cpu_baseline"] = cpu_baseline(w)
+        line["parity"] = parity_vs_oracle(w, d, ref)
     if rank == 0 and ws == 1 and not args.no_sweep:
         del d, w
         torch.cuda.empty_cache()
