@@ -726,6 +726,8 @@ def main():
         "clocks": clocks.summary(),
     }
     line.update(extras)
+    if "read_probe" in line:
+        line["read_probe"]["scoring_kernel_ratio"] = line["logits_GBps"] / line["read_probe"]["GBps"]
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -771,6 +773,15 @@ def variant_legs(ps, w, d, dev, stream, steps: int, logits_bytes: int) -> dict:
                                                 stream, entropy=ent_rows))))
     st = int(d.t["status"].item())
     assert st == 0, ps.dev_status_names(st)
+    # a plain streaming read of the same logits buffer on the same box: the
+    # read rate the scoring kernel's own rate is compared with
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    read_ms = kernel_loop(stream, steps, lambda: ps.ps_selftest_read(w.logits, sink, stream))
+    read_bytes = w.logits.numel() * w.logits.element_size()
+    out["read_probe"] = {"kernel_ms": read_ms, "GBps": read_bytes / (read_ms / 1e3) / 1e9,
+                         "bytes": read_bytes,
+                         "how": "ps_selftest_read: 16-byte streaming loads, 8 in flight per "
+                                "thread, 4 x 512 threads per SM, over the batch's logits"}
     # the round carry-over (reached state's per-position values) after a step
     lay = w.layout
     n_ch, T = lay.n_chains, lay.T

@@ -472,6 +472,19 @@ double ps_midpoint_branch_probability(double p_accept, double p_reject);
  */
 ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status, void *cuda_stream);
 
+/*
+ * Diagnostic with no counterpart in the PreSTO pages: reads `bytes` of device
+ * memory at `data` once, with 16-byte streaming loads spread over every SM,
+ * and folds the words into *sink with XOR.  Timing it gives the plain read
+ * rate of the device, to which the scoring kernel's rate can be compared.
+ *
+ * data    device memory, 16-byte aligned.
+ * bytes   a multiple of 16 (else PS_ERR_INVALID_ARG); 0 launches nothing.
+ * sink    device uint32 word; its value is meaningless beyond keeping the
+ *         loads.
+ */
+ps_status ps_selftest_read(const void *data, size_t bytes, uint32_t *sink, void *cuda_stream);
+
 /* Static text for a status code. */
 const char *ps_status_string(ps_status status);
 

@@ -136,6 +136,8 @@ def lib() -> ctypes.CDLL:
         L.ps_validate_subtree.restype = ctypes.c_int
         L.ps_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp, _vp]
         L.ps_selftest_wait_timeout.restype = ctypes.c_int
+        L.ps_selftest_read.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
+        L.ps_selftest_read.restype = ctypes.c_int
         L.ps_status_string.argtypes = [ctypes.c_int]
         L.ps_status_string.restype = ctypes.c_char_p
         L.ps_version.argtypes = []
@@ -227,6 +229,19 @@ def ps_selftest_wait_timeout(limit_ns: int, status: torch.Tensor, stream=None,
     st = lib().ps_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream(stream, status))
     if check and st != PS_OK:
         raise PsError(st, "ps_selftest_wait_timeout")
+    return st
+
+
+def ps_selftest_read(data: torch.Tensor, sink: torch.Tensor, stream=None,
+                     check: bool = True) -> int:
+    """Diagnostic: one plain streaming read of `data` (a contiguous device
+    tensor, 16-byte aligned, a multiple of 16 bytes), folded into the int32
+    `sink`; timing it gives the device's plain read rate (see include/ps.h)."""
+    _need(sink, torch.int32, "sink")
+    nbytes = data.numel() * data.element_size()
+    st = lib().ps_selftest_read(_ptr(data), nbytes, _ptr(sink), _stream(stream, data))
+    if check and st != PS_OK:
+        raise PsError(st, "ps_selftest_read")
     return st
 
 

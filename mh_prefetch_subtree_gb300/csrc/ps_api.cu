@@ -615,6 +615,16 @@ extern "C" ps_status ps_selftest_wait_timeout(uint64_t limit_ns, int32_t *status
     return map_cuda(ps::launch_wait_selftest(limit_ns, status, (cudaStream_t)cuda_stream));
 }
 
+extern "C" ps_status ps_selftest_read(const void *data, size_t bytes, uint32_t *sink,
+                                      void *cuda_stream) {
+    if (!data || !sink || !aligned(data, 16) || bytes % 16 != 0) return PS_ERR_INVALID_ARG;
+    int sms = 0;
+    ps_status st = device_of(data, &sms);
+    if (st != PS_OK) return st;
+    return map_cuda(ps::launch_read_probe(data, (int64_t)(bytes / 16), sink, sms,
+                                          (cudaStream_t)cuda_stream));
+}
+
 extern "C" ps_status ps_carry_state(const ps_subtree_batch *b, const ps_carry_io *io,
                                       void *cuda_stream) {
     if (!b || !io || b->T < 1 || b->n_chains < 1 || b->n_seg < b->n_chains || b->n_rows < 0)

@@ -126,6 +126,9 @@ cudaError_t launch_carry(const CarryParams &p, cudaStream_t stream);
 size_t score_rows_smem_bytes();
 // Diagnostic: a bounded wait on an mbarrier that nothing completes.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t *status, cudaStream_t stream);
+// Diagnostic: a plain streaming read of n_vec 16-byte words, folded into *sink.
+cudaError_t launch_read_probe(const void *data, int64_t n_vec, uint32_t *sink, int sms,
+                              cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers

@@ -241,3 +241,14 @@ def test_batch_flags_need_no_gpu():
     assert ps.ps_score_rows(b, lp0, lq, st, ws, stream=0, check=False) == 7
     b.flags = 0x2                               # an unknown bit
     assert ps.ps_score_rows(b, lp0, lq, st, ws, stream=0, check=False) == 1
+
+
+def test_read_probe_host_checks_need_no_gpu():
+    import torch
+    sink = torch.zeros(1, dtype=torch.int32)
+    data = torch.zeros(64, dtype=torch.uint8)
+    # a size that is not a multiple of 16 bytes, and a misaligned start
+    assert ps.ps_selftest_read(data[:40], sink, stream=0, check=False) == 1
+    assert ps.ps_selftest_read(data[4:36], sink, stream=0, check=False) == 1
+    # a host pointer is not device memory
+    assert ps.ps_selftest_read(data[:32], sink, stream=0, check=False) == 1

@@ -1,5 +1,7 @@
-"""Failure detection on the GPU without a fault: a bounded device wait that
-nothing completes ends with PS_DEV_TIMEOUT, and the context stays usable."""
+"""Diagnostics on the GPU.  Failure detection without a fault: a bounded
+device wait that nothing completes ends with PS_DEV_TIMEOUT, and the context
+stays usable.  The plain-read probe that the bench times reads every word of
+its buffer once."""
 
 import time
 
@@ -40,3 +42,19 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ps.ps_selftest_wait_timeout(2_000_000, st2, side)
     torch.cuda.synchronize()
     assert int(st2.item()) == PS_DEV_TIMEOUT
+
+
+def test_read_probe_reads_every_word_once():
+    # the plain-read diagnostic folds every 32-bit word of the buffer with XOR:
+    # equal to numpy's fold over the same bytes, for a buffer whose length is
+    # not a multiple of the probe's stride
+    import numpy as np
+    g = torch.Generator(device="cuda:0")
+    g.manual_seed(7)
+    n = (1 << 20) * 37 + 12
+    x = torch.randint(-2**31, 2**31 - 1, (n,), dtype=torch.int32, device="cuda:0", generator=g)
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    ps.ps_selftest_read(x, sink)
+    torch.cuda.synchronize()
+    want = np.bitwise_xor.reduce(x.cpu().numpy().view(np.uint32))
+    assert int(sink.cpu().numpy().view(np.uint32)[0]) == int(want)
