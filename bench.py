@@ -773,6 +773,26 @@ def variant_legs(ps, w, d, dev, stream, steps: int, logits_bytes: int) -> dict:
                                                 stream, entropy=ent_rows))))
     st = int(d.t["status"].item())
     assert st == 0, ps.dev_status_names(st)
+    # a masked vocabulary (all but the first 1000 ids at -inf, tokens among
+    # them) in the entropy variant, without and with the masked-logits hint
+    masked = w.logits.clone()
+    masked[:, 1000:] = float("-inf")
+    mtok = (w.tokens % 1000).to(torch.int32)
+    mb = {flags: ps.make_batch(V=w.V, T=w.layout.T, alpha=w.alpha, tau=w.tau,
+                               chain_seg0=d.t["chain_seg0"], seg_row0=d.t["seg_row0"],
+                               seg_cut=d.t["seg_cut"], seg_src=d.t["seg_src"], logits=masked,
+                               tokens=mtok, flags=flags)
+          for flags in (0, ps.PS_FLAG_MASKED_LOGITS)}
+    out["masked_vocabulary_with_entropy"] = {
+        "no_hint": rate(kernel_loop(stream, steps, lambda: ps.ps_score_rows(
+            mb[0], lp0_v, lq_v, d.t["status"], d.workspace, stream, entropy=ent_rows))),
+        "masked_logits_hint": rate(kernel_loop(stream, steps, lambda: ps.ps_score_rows(
+            mb[ps.PS_FLAG_MASKED_LOGITS], lp0_v, lq_v, d.t["status"], d.workspace, stream,
+            entropy=ent_rows))),
+        "vocabulary": "all but the first 1000 ids at -inf"}
+    del masked, mb
+    st = int(d.t["status"].item())
+    assert st == 0, ps.dev_status_names(st)
     # a plain streaming read of the same logits buffer on the same box: the
     # read rate the scoring kernel's own rate is compared with
     sink = torch.zeros(1, dtype=torch.int32, device=dev)
