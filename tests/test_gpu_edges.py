@@ -142,3 +142,24 @@ def test_carry_with_a_foreign_state_is_flagged():
     torch.cuda.synchronize()
     assert int(out["status"].item()) & 0x10
     assert torch.isnan(out["lp0"][1]).all() and torch.isfinite(out["lp0"][0]).all()
+
+
+def test_chain_larger_than_the_walks_shared_memory_stage():
+    # one chain of 300 requests: 1,669 nodes and 301 segments, more than the
+    # walk stages in shared memory (512 nodes, 256 segments), so it walks from
+    # global memory; against the oracle through the one-call round, and the
+    # walk kernel of ps_walk_subtree gives the same path
+    import mh_prefetch_subtree_gb300 as ps
+    rng = np.random.default_rng(69)
+    w = _workload([bfs_tree(rng, 64, 300)], 1024, dtype="f32", seed=69, max_steps=100)
+    lay = w.layout
+    assert len(lay.acc) > 512 and lay.n_seg > 256
+    s = H.full_parity(w)
+    d = ps.DeviceSubtree.create(layout=lay, u=w.u, logits=w.logits, tokens=w.tokens, V=w.V,
+                                alpha=w.alpha, tau=w.tau, max_steps=w.max_steps)
+    d.step(fused=False)
+    torch.cuda.synchronize()
+    g = H.run_gpu(w)
+    for k in ("state_seg", "end_node", "k_delta", "path"):
+        assert np.array_equal(d.t[k].cpu().numpy(), g[k]), k
+    assert s["k_delta_mean"] >= 1
