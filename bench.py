@@ -210,11 +210,12 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def cpu_baseline(w, max_seconds: float = 30.0) -> dict:
+def cpu_baseline(w, max_seconds: float = 30.0) -> tuple[dict, dict]:
     """The oracle, as it stands, on the same batch: per-row log-probabilities
     (the step computes no entropy, so neither does this), the suffix sums over
     explicit states, log A and the walk, on all host cores; and the per-row
-    part on one core over a sample of rows, extrapolated to the batch."""
+    part on one core over a sample of rows, extrapolated to the batch.
+    Returns the oracle's results (for the parity check) and the record."""
     import oracle
     from oracle.hostcopy import oracle_rows     # block-wise host copies for the oracle
     threads = oracle.default_threads()
