@@ -30,8 +30,11 @@
  * Ownership: every pointer passed to the GPU calls is device memory owned by
  * the caller, including the workspace.  The library allocates no device
  * memory, keeps no per-call state and is safe to call from several host
- * threads on different streams.  Calls are asynchronous on the given stream
- * (a cudaStream_t passed as void*, NULL = the legacy default stream), with
+ * threads on different streams, each call with its own workspace and outputs
+ * (calls that share a workspace must be ordered on one stream: they use it as
+ * scratch, and its counters start from zero at each call).  Calls are
+ * asynchronous on the given stream (a cudaStream_t passed as void*, NULL =
+ * the legacy default stream), with
  * plain stream order: each call sees everything enqueued on the stream before
  * it, including the caller's own kernels that write its inputs.  (Some kernels
  * are launched so that they start while the previous kernel finishes; they
