@@ -34,9 +34,9 @@
  * (calls that share a workspace must be ordered on one stream: they use it as
  * scratch, and its counters start from zero at each call).  Calls are
  * asynchronous on the given stream (a cudaStream_t passed as void*, NULL =
- * the legacy default stream), with
- * plain stream order: each call sees everything enqueued on the stream before
- * it, including the caller's own kernels that write its inputs.  (Some kernels
+ * the legacy default stream), with plain stream order: each call sees
+ * everything enqueued on the stream before it, including the caller's own
+ * kernels that write its inputs.  (Some kernels
  * are launched so that they start while the previous kernel finishes; they
  * read no input before that kernel's writes are visible.)
  *
