@@ -794,6 +794,11 @@ def variant_legs(ps, w, d, dev, stream, steps: int, logits_bytes: int) -> dict:
     del masked, mb
     st = int(d.t["status"].item())
     assert st == 0, ps.dev_status_names(st)
+    # the kernels after scoring on their own (the round runs them as one
+    # kernel): ps_assemble_subtree and ps_walk_subtree back to back
+    out["after_scoring_kernels_alone"] = {
+        "suffix_sums_us": kernel_loop(stream, steps, lambda: d.assemble(stream)) * 1e3,
+        "walk_us": kernel_loop(stream, steps, lambda: d.walk(stream)) * 1e3}
     # a plain streaming read of the same logits buffer on the same box: the
     # read rate the scoring kernel's own rate is compared with
     sink = torch.zeros(1, dtype=torch.int32, device=dev)
