@@ -116,7 +116,8 @@ def _small(V, dtype, T=12, n_pf=5, tau=0.25, alpha=4.0, n_chains=2, seed=0, kind
 @pytest.mark.parametrize("V,dtype,ld", [
     (1, "f32", 4), (2, "bf16", 8), (7, "bf16", 8), (1000, "bf16", 1008), (1000, "f32", 1000),
     (2048, "bf16", None), (2056, "bf16", None), (4097, "f32", 4100), (151936, "bf16", None),
-    (262144, "bf16", None), (65536 + 24, "bf16", 65536 + 32)])
+    (262144, "bf16", None), (65536 + 24, "bf16", 65536 + 32), (151936, "f32", None),
+    (151937, "bf16", 151944)])
 def test_vocab_shapes_and_padding(V, dtype, ld):
     # NaN padding beyond V must be ignored (it is patched to -inf in shared memory);
     # a one-token vocabulary cannot hold a boosted token, so it uses plain rows
