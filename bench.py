@@ -592,7 +592,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the 36-point throughput sweep alone, one line per point")
     ap.add_argument("--sweep-steps", type=int, default=2)
-    ap.add_argument("--sweep-warmup", type=int, default=1)
+    ap.add_argument("--sweep-warmup", type=int, default=3)
     ap.add_argument("--sweep-points", type=int, default=None,
                     help="with --sweep: time only the first K points (for profiling runs)")
     ap.add_argument("--n-pf", type=int, default=None,
