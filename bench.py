@@ -280,6 +280,39 @@ def parity_vs_oracle(w, d, ref) -> dict:
     return out
 
 
+def reference_sample_tree(tree, row_budget: int):
+    """A sample of one chain's subtree with at most about row_budget rows.
+
+    Normally the root's rows and the first requests in order, request rows up
+    to min(2,500, row_budget - root rows), at least one request.  When the
+    root and the first request alone exceed row_budget, the sample is one
+    request of the tree proposed from the root: the longest suffix whose two
+    segments (root rows c+1..T and the request's) fit the budget, else the
+    shortest one, with the root's cut raised to that request's cut.
+    """
+    from synth.trees import ChainTree
+    T = tree.T
+    root_rows = T - tree.seg_cut[0]
+    cuts = tree.seg_cut[1:]
+    if not cuts or root_rows + T - cuts[0] <= row_budget:
+        budget = min(2500, row_budget - root_rows)
+        keep, req_rows = 1, 0
+        while keep < len(tree.seg_cut) and (
+                keep == 1 or req_rows + T - tree.seg_cut[keep] <= budget):
+            req_rows += T - tree.seg_cut[keep]
+            keep += 1
+        tree.seg_cut = tree.seg_cut[:keep]
+        tree.seg_src = tree.seg_src[:keep]
+        tree.req = [r if r < keep else -1 for r in tree.req]
+        return tree
+    fit = [c for c in cuts if 2 * (T - c) <= row_budget]
+    c = min(fit) if fit else max(cuts)
+    t = ChainTree.new(T)
+    t.expand(0, c)
+    t.finalize_root_cut()
+    return t
+
+
 def reference_arm(args, ws, rank):
     """--impl reference: the CPU oracle timed as the step, on bounded samples."""
     if rank != 0:
@@ -290,24 +323,18 @@ def reference_arm(args, ws, rank):
     w = make_workload(args.config, device="cpu") if args.config == 1 else None
     tokens_per_row = None               # of the full batch, when w is a sample of it
     if w is None:
-        # a bounded sample of the same batch: the same tree, with the root's
-        # rows and the rows of its first requests only (at least one request,
-        # and up to 2,500 request rows: about a second of oracle work)
+        # a bounded sample of the same batch, sized so that the whole run stays
+        # near 90 s at about 7,000 oracle rows/s on 16 cores (and a step at
+        # most the root's rows + 2,500 request rows); tokens are credited at
+        # the full batch's suffix tokens per row
         from synth.workload import CONFIGS, _trees_for, draw_tokens, gen_logits, Workload
         cfg = dict(CONFIGS[args.config])
         rng = np.random.default_rng(10086 + args.config)
         tree = _trees_for(cfg, rng)[0]
         full = assemble_layout([tree])
         tokens_per_row = full.suffix_tokens() / full.n_rows
-        keep = 1
-        req_rows = 0
-        while keep < len(tree.seg_cut) and (
-                keep == 1 or req_rows + tree.T - tree.seg_cut[keep] <= 2500):
-            req_rows += tree.T - tree.seg_cut[keep]
-            keep += 1
-        tree.seg_cut = tree.seg_cut[:keep]
-        tree.seg_src = tree.seg_src[:keep]
-        tree.req = [r if r < keep else -1 for r in tree.req]
+        root_cut0 = tree.seg_cut[0]
+        tree = reference_sample_tree(tree, 90 * 7000 // max(1, args.steps + args.warmup))
         lay = assemble_layout([tree])
         x = gen_logits(cfg["logits"][0], cfg["logits"][1], lay.n_rows, cfg["V"], cfg["dtype"],
                        seed=1, device="cpu")
@@ -339,7 +366,9 @@ def reference_arm(args, ws, rank):
         how = f"the whole batch ({w.n_rows} rows) per step"
     else:
         units_per_step = w.n_rows * tokens_per_row
-        how = (f"{w.n_rows} rows of the batch per step (the root's and its first requests'); "
+        which = ("the root's and its first requests'" if w.layout.seg_cut[0] == root_cut0
+                 else "one request proposed from the root and the root's rows it reads")
+        how = (f"{w.n_rows} rows of the batch per step ({which}); "
                f"tokens = rows x the batch's {tokens_per_row:.4f} suffix tokens per row")
     v = units_per_step * args.steps / el
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
