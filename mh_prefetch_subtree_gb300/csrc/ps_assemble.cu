@@ -46,8 +46,10 @@ __device__ __forceinline__ double warp_sum(double v) {
 // range 0 (the y rows) goes to (a, b), ranges 1-3 (the x suffix) to (e, f).
 // Range k reads lp_k[o_k + j], lq_k[o_k + j] for j < n_k.  The threads stride
 // over the index space and issue the loads of up to kU indices before adding
-// any, so a request's sums usually take one round of memory latency.  Each
-// thread adds its elements in index order: the result is deterministic.
+// any (2,048 indices per round for the block), so a request's sums usually
+// take one or two rounds of memory latency.  Each thread adds its elements in
+// index order: the result is deterministic.  (Deeper rounds, 12 or 16 loads
+// per thread, measured slower: they take more registers per thread.)
 struct Ranges {
     const double *lp[4];
     const double *lq[4];
@@ -90,6 +92,19 @@ __device__ __forceinline__ void ranges_sum(const Ranges &g, int tid, double &a, 
     }
 }
 
+// Adds 1 to *cnt with release and acquire semantics at GPU scope and returns
+// the old value: the caller's earlier writes are visible to whichever thread
+// later sees the sum, and the writes of the threads whose additions came
+// before are visible to the caller.
+__device__ __forceinline__ int32_t arrive_acq_rel(int32_t *cnt) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(cnt)
+                 : "memory");
+    return old;
+}
+
 // Chain holding segment s: the last c with chain_seg0[c] <= s.
 __device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
     int lo = 0, hi = n_chains - 1;
@@ -106,12 +121,17 @@ __device__ int chain_of(const int32_t *chain_seg0, int n_chains, int32_t s) {
 // also walks that chain with its first warp, so that the walk needs no launch
 // of its own.  EARLY: the kernel directly follows libps's own scoring kernel,
 // launched in the same call, so the caller's inputs were written before that
-// kernel started and the metadata may be loaded before griddepcontrol.wait;
-// only the per-row values wait.  Without EARLY nothing is read before the
-// wait, because the previous kernel may be the caller's own kernel writing
-// the layout arrays.
+// kernel started and the metadata may be loaded before griddepcontrol.wait
+// (with FUSED, every CTA's first warp also stages its chain's tree and
+// uniforms then, in case it is the one that walks); only the per-row values
+// wait.  Without EARLY nothing is read before the wait, because the previous
+// kernel may be the caller's own kernel writing the layout arrays.
+//
+// The early fused form holds its chain's bounds through the sums; its bound of
+// three CTAs per SM keeps it at the occupancy of the others (at most 85
+// registers a thread), which matters when a batch has thousands of segments.
 template <bool FUSED, bool EARLY>
-__global__ void __launch_bounds__(kAssembleThreads)
+__global__ void __launch_bounds__(kAssembleThreads, (FUSED && EARLY) ? 3 : 0)
     assemble_kernel(const AssembleParams p, const WalkParams wp, int32_t *chain_cnt) {
     constexpr int kWarps = kAssembleThreads / 32;
     __shared__ double red[4][kWarps];
@@ -125,6 +145,10 @@ __global__ void __launch_bounds__(kAssembleThreads)
     pdl_launch_dependents();                         // the next kernel may be scheduled now
     if constexpr (!EARLY) pdl_wait_prerequisites();
     const int c = chain_of(p.chain_seg0, p.n_chains, s);
+    ChainStage stage{};
+    if constexpr (FUSED && EARLY) {
+        if (warp == 0) stage = stage_chain(wp, c, wsm, lane);
+    }
     // metadata in two rounds of loads: what depends on s (and c) only, then
     // the root's and src's entries (indices clamped in range, checked below)
     const int32_t s0 = p.chain_seg0[c];
@@ -211,6 +235,11 @@ __global__ void __launch_bounds__(kAssembleThreads)
             }
         }
     }
+    // a chain root reads no per-row value, but it waits as well, so that no CTA
+    // of this kernel ends before the scoring kernel has
+    if constexpr (EARLY) {
+        if (root) pdl_wait_prerequisites();
+    }
     if (tid == 0) {
         if (bits) set_status(p.status, bits);
         if (root) {
@@ -239,19 +268,16 @@ __global__ void __launch_bounds__(kAssembleThreads)
     if constexpr (FUSED) {
         // the last CTA of the chain to get here walks it (a chain whose
         // chain_seg0 bounds failed the checks above is not counted, so not
-        // walked; its status bit is set)
-        if (tid == 0) {
-            int last = 0;
-            if (chain_ok) {
-                __threadfence();                      // this CTA's log A before its arrival
-                last = atomicAdd(chain_cnt + c, 1) == s1 - s0 - 1;
-            }
-            walk_here = last;
-        }
+        // walked; its status bit is set).  Thread 0 wrote this CTA's outputs:
+        // its release publishes them, and the last arrival's acquire, passed
+        // on by the barrier, makes every arrival's log A visible to the warp
+        // that walks.
+        if (tid == 0)
+            walk_here = chain_ok && arrive_acq_rel(chain_cnt + c) == s1 - s0 - 1;
         __syncthreads();
-        if (walk_here) {
-            __threadfence();                          // every arrival's log A is visible
-            if (warp == 0) walk_chain(wp, c, wsm, lane);
+        if (walk_here && warp == 0) {
+            if constexpr (!EARLY) stage = stage_chain(wp, c, wsm, lane);
+            walk_staged(wp, c, stage, wsm, lane);
         }
     }
 }

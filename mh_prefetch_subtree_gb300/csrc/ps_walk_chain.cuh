@@ -49,14 +49,45 @@ __device__ __forceinline__ int8_t decide(double u, double la) {
     return u <= exp(la) ? 1 : 0;
 }
 
-// Walks chain c (0 <= c < n_chains) with the calling warp; all 32 lanes call
-// it, after the tree, the uniforms and log A are visible to them.
-__device__ __forceinline__ void walk_chain(const WalkParams &p, int c, WalkSmem &w, int lane) {
+// Chain c's bounds and, when the chain fits, its node arrays and its
+// requests' uniforms in shared memory.  All 32 lanes call it and get the same
+// result; the copies are visible to the warp after a __syncwarp().
+struct ChainStage {
+    int32_t n0, n1, s0, s1;
+    bool ok;        // the bounds are consistent
+    bool staged;    // the node arrays and uniforms are in shared memory
+};
+
+__device__ __forceinline__ ChainStage stage_chain(const WalkParams &p, int c, WalkSmem &w,
+                                                  int lane) {
+    ChainStage g;
+    g.n0 = p.chain_node0[c];
+    g.n1 = p.chain_node0[c + 1];
+    g.s0 = p.chain_seg0[c];
+    g.s1 = p.chain_seg0[c + 1];
+    g.ok = !(g.n0 < 0 || g.n1 > p.n_nodes || g.n1 <= g.n0 || g.s0 < 0 || g.s1 > p.n_seg ||
+             g.s1 <= g.s0);
+    g.staged = g.ok && g.n1 - g.n0 <= kNodeCap && g.s1 - g.s0 <= kSegCap;
+    if (g.staged) {
+        for (int i = lane; i < g.n1 - g.n0; i += 32) {
+            w.acc[i] = p.acc[g.n0 + i];
+            w.rej[i] = p.rej[g.n0 + i];
+            w.req[i] = p.req[g.n0 + i];
+        }
+        for (int i = lane; i < g.s1 - g.s0; i += 32) w.u[i] = p.u[g.s0 + i];
+    }
+    return g;
+}
+
+// Walks chain c (0 <= c < n_chains) with the calling warp, given what
+// stage_chain() returned for it; all 32 lanes call it, after log A is visible
+// to them.
+__device__ __forceinline__ void walk_staged(const WalkParams &p, int c, const ChainStage &g,
+                                            WalkSmem &w, int lane) {
     const int stride = p.max_steps + 1;
     int32_t *path = p.path ? p.path + (int64_t)c * stride : nullptr;
-    const int32_t n0 = p.chain_node0[c], n1 = p.chain_node0[c + 1];
-    const int32_t s0 = p.chain_seg0[c], s1 = p.chain_seg0[c + 1];
-    if (n0 < 0 || n1 > p.n_nodes || n1 <= n0 || s0 < 0 || s1 > p.n_seg || s1 <= s0) {
+    const int32_t n0 = g.n0, n1 = g.n1, s0 = g.s0, s1 = g.s1;
+    if (!g.ok) {
         if (lane == 0) {
             set_status(p.status, PS_DEV_BAD_TREE);
             p.state_seg[c] = -1;
@@ -67,18 +98,12 @@ __device__ __forceinline__ void walk_chain(const WalkParams &p, int c, WalkSmem 
             for (int i = lane; i < stride; i += 32) path[i] = -1;
         return;
     }
-    const int32_t nn = n1 - n0, ns = s1 - s0;
-    const bool staged = nn <= kNodeCap && ns <= kSegCap;
+    const int32_t nn = n1 - n0;
+    const bool staged = g.staged;
     if (staged) {
-        for (int i = lane; i < nn; i += 32) {
-            w.acc[i] = p.acc[n0 + i];
-            w.rej[i] = p.rej[n0 + i];
-            w.req[i] = p.req[n0 + i];
-        }
-        for (int i = lane; i < ns; i += 32) w.u[i] = p.u[s0 + i];
         // each request's decision, taken by all lanes at once so that the walk
-        // below only follows it
-        for (int i = lane; i < ns; i += 32)
+        // below only follows it (a lane reads the uniforms it staged itself)
+        for (int i = lane; i < s1 - s0; i += 32)
             w.acc_dec[i] = decide(w.u[i], __ldcg(p.log_accept + s0 + i));
     }
     if (path)
@@ -125,6 +150,12 @@ __device__ __forceinline__ void walk_chain(const WalkParams &p, int c, WalkSmem 
     p.state_seg[c] = state;
     p.end_node[c] = v;
     p.k_delta[c] = k;
+}
+
+// Stages and walks chain c in one go (all 32 lanes call it).
+__device__ __forceinline__ void walk_chain(const WalkParams &p, int c, WalkSmem &w, int lane) {
+    const ChainStage g = stage_chain(p, c, w, lane);
+    walk_staged(p, c, g, w, lane);
 }
 
 }  // namespace
