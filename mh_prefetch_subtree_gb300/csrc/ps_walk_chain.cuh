@@ -33,8 +33,10 @@ struct WalkSmem {
 
 // The accept test of Algorithm 1, u <= A with A = exp(log A): 1 accept,
 // 0 reject, -1 the uniform is outside (0, 1].  A float exponential settles it
-// unless u is within 1e-5 (relative) of A or A is below float range; then the
-// float64 exponential decides.  A NaN log A rejects.
+// unless u is within 1e-5 (relative) of A; below log A = -80, A < 1.9e-35, so
+// every u >= 1e-30 rejects.  Only the rest (a near tie, or a tiny u) takes the
+// float64 exponential, which is slow on this GPU's float64 pipe.  A NaN log A
+// rejects.
 __device__ __forceinline__ int8_t decide(double u, double la) {
     if (!(u > 0.0 && u <= 1.0)) return -1;
     if (!(la == la)) return 0;
@@ -45,6 +47,8 @@ __device__ __forceinline__ int8_t decide(double u, double la) {
         const double a = (double)expf((float)la);
         if (u < a * (1.0 - 1e-5)) return 1;
         if (u > a * (1.0 + 1e-5)) return 0;
+    } else if (u >= 1e-30) {
+        return 0;
     }
     return u <= exp(la) ? 1 : 0;
 }

@@ -5,6 +5,8 @@ log-probabilities within 1e-4 relative, log A within 1e-3 absolute, and the
 walk exactly (near-ties excepted, see tests/gpu_harness.py).
 """
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -361,6 +363,40 @@ def test_walk_brute_force_patterns():
         for c in range(lays.n_chains):
             assert list(g["path"][c * 101:c * 101 + o["k_delta"][c] + 1]) == o["path"][c]
         checked += 1
+
+
+def test_walk_decisions_at_tiny_acceptance_probabilities():
+    # one request per chain, log A and u chosen around the walk's shortcuts:
+    # below log A = -80 every u >= 1e-30 rejects without an exponential; a
+    # smaller u, or a u within 1e-5 of A, is settled by the float64 one
+    from synth.trees import ChainTree
+    cases = [(-85.0, 1e-30), (-85.0, 0.5), (-85.0, math.exp(-86.0)), (-85.0, math.exp(-84.0)),
+             (-80.0, 1e-30), (-80.0, math.exp(-80.0) * (1 - 1e-9)),
+             (-79.9, math.exp(-79.9) * (1 - 1e-6)), (-79.9, math.exp(-79.9) * (1 + 1e-6)),
+             (-200.0, 1e-300), (-700.0, 1e-300), (-700.0, 1e-305), (-745.0, 1e-320),
+             (-math.inf, 5e-324),
+             (-1e-12, 1.0), (-3.0, math.exp(-3.0) * (1 - 1e-7))]
+    trees = []
+    for _ in cases:
+        t = ChainTree.new(16)
+        t.expand(0, 5)
+        t.finalize_root_cut()
+        trees.append(t)
+    lay = assemble_layout(trees)
+    la = np.full(lay.n_seg, np.nan)
+    u = np.ones(lay.n_seg)
+    for c, (a, x) in enumerate(cases):
+        la[2 * c + 1], u[2 * c + 1] = a, x
+    g = _walk_only(lay, la, u, 10)
+    o = oracle.walk(lay, la, u, 10)
+    assert g["status"][0] == 0
+    want = np.array([1 if x <= math.exp(a) else 0 for a, x in cases])
+    assert list(want) == [0, 0, 1, 0, 0, 1, 1, 0, 1, 0, 1, 0, 0, 0, 1]
+    assert np.array_equal(o["k_delta"], np.ones(len(cases)))
+    accepted = g["state_seg"] == np.arange(len(cases)) * 2 + 1
+    assert np.array_equal(accepted.astype(int), want)
+    assert np.array_equal(g["state_seg"], o["state_seg"])
+    assert np.array_equal(g["end_node"], o["end_node"])
 
 
 def test_walk_max_steps_deferred_and_cycle():
