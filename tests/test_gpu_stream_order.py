@@ -11,7 +11,6 @@ section 3.2 step (3) and eq. (6)).  The same holds for ps_score_walk_subtree,
 whose suffix-sum + walk kernel reads the layout early.
 """
 
-import numpy as np
 import pytest
 import torch
 
