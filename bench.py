@@ -602,6 +602,22 @@ def kernel_loop(stream, steps: int, fn) -> float:
     return a.elapsed_time(b) / steps
 
 
+def tail_after_scoring(d, stream, reps: int = 7, loop_ms: float = 250.0) -> dict:
+    """What a round adds after its scoring kernel: rounds and scoring-kernel
+    launches timed in alternating back-to-back loops of the same length, the
+    median of the per-repetition differences.  Interleaving keeps slow drifts
+    of the read rate out of the difference."""
+    k1 = kernel_loop(stream, 3, lambda: d.score_rows(stream))
+    n = max(20, min(2000, int(loop_ms / max(k1, 1e-3))))
+    diffs = []
+    for _ in range(reps):
+        r = kernel_loop(stream, n, lambda: d.step(stream))
+        k = kernel_loop(stream, n, lambda: d.score_rows(stream))
+        diffs.append((r - k) * 1e3)
+    return {"median_us": float(np.median(diffs)), "min_us": float(min(diffs)),
+            "max_us": float(max(diffs)), "reps": reps, "rounds_per_loop": n}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -684,6 +700,7 @@ def main():
     # the scoring kernel alone, back to back on the same stream, for its roofline
     k1_avg = kernel_loop(stream, args.steps, lambda: d.score_rows(stream))
     clocks.mark(False)
+    tail = tail_after_scoring(d, stream)
     if ws > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), dev)
@@ -752,7 +769,9 @@ def main():
         "kernel_launches_per_step": {"score_rows_kernel": 1,
                                      "assemble_kernel (suffix sums, log A and the walk)": 1},
         # what the suffix sums, log A and the walk add to a step after scoring
-        "after_scoring_us": (ms_per_step - k1_avg) * 1e3,
+        "after_scoring_us": tail["median_us"],
+        "after_scoring": dict(tail, how="median over alternating loops of rounds and of the "
+                                        "scoring kernel alone"),
         "clocks": clocks.summary(),
     }
     line.update(extras)
