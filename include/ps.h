@@ -37,8 +37,11 @@
  * the legacy default stream), with plain stream order: each call sees
  * everything enqueued on the stream before it, including the caller's own
  * kernels that write its inputs.  (Some kernels
- * are launched so that they start while the previous kernel finishes; they
- * read no input before that kernel's writes are visible.)
+ * are launched so that they may start while the previous kernel finishes;
+ * they read nothing until that kernel's writes are visible, except the second
+ * kernel of ps_score_walk_subtree, which reads the segment arrays, the tree
+ * and the uniforms early: those were complete before that call's own first
+ * kernel began.)
  *
  * Errors: the returned ps_status reports what the host can check without
  * reading device memory (sizes, null pointers, alignment, launch failures).
