@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -32,11 +33,11 @@ WsLayout ws_layout(int64_t n_rows, int32_t n_chains) {
     w.rows_off = 0;
     w.rows_bytes = align_up((size_t)(n_rows > 0 ? n_rows : 0) * 2 * sizeof(double), kAlign);
     w.parts_off = w.rows_off + w.rows_bytes;
-    w.parts_bytes = align_up((size_t)2 * ps::kMaxWarps * sizeof(ps::RowPart), kAlign);
+    w.parts_bytes = align_up((size_t)2 * ps::kMaxRanges * sizeof(ps::RowPart), kAlign);
     w.chain_cnt_off = w.parts_off + w.parts_bytes;
     w.chain_cnt_bytes = align_up((size_t)(n_chains > 0 ? n_chains : 0) * sizeof(int32_t), kAlign);
     w.cnt_off = w.chain_cnt_off + w.chain_cnt_bytes;
-    w.cnt_bytes = align_up((size_t)ps::kMaxWarps * sizeof(int32_t), kAlign);
+    w.cnt_bytes = align_up((size_t)ps::kMaxRanges * sizeof(int32_t), kAlign);
     w.total = w.cnt_off + w.cnt_bytes;
     return w;
 }
@@ -140,13 +141,14 @@ size_t ps_score_workspace_bytes(const ps_subtree_batch *batch) {
 namespace {
 
 // Where the row kernel keeps its scratch: the split-row partials, the arrival
-// counters, and how many warps (one partial pair and one counter each) fit.
-// The memset before the launch clears [zero_from, counters + warps), so that
-// counters placed just before the row kernel's are cleared with them.
+// counters, and how many chunk ranges (one partial pair and one counter each)
+// fit; one counter slot goes to the tail-block claim counter.  The memset
+// before the launch clears [zero_from, the claim counter], so that counters
+// placed just before the row kernel's are cleared with them.
 struct RowsScratch {
     ps::RowPart *parts;
     int32_t *counters;
-    int64_t max_warps;
+    int64_t max_ranges;
     int32_t *zero_from;
 };
 
@@ -174,9 +176,29 @@ ps_status launch_rows(const ps_subtree_batch *b, int sms, const RowsScratch &scr
     p.cpr = (p.row_bytes + ps::kStageBytes - 1) / ps::kStageBytes;
     p.n_chunks = b->n_rows * p.cpr;
     int64_t warps = (int64_t)sms * ps::kWarpsPerCta;
-    if (warps > scr.max_warps) warps = scr.max_warps;
+    if (warps > scr.max_ranges - 1) warps = scr.max_ranges - 1;
     if (warps > p.n_chunks) warps = p.n_chunks;
     p.n_vwarps = (int32_t)warps;
+    // On batches where each warp streams at least kTailMinShare chunks, static
+    // ranges cover the first 15/16 of the chunks and the last 1/16 is cut
+    // into tail blocks (up to 8 per warp, as the scratch allows, of at least
+    // kTailMinBlock chunks) that the warps finishing first take, so that a
+    // slow SM does not set the end.  On smaller batches a block would take
+    // about as long as the spread between SMs, and claiming it and refilling
+    // the ring cost more than it saves.  The entropy variants have no tail
+    // blocks (the kernel's kTail).
+    constexpr int64_t kTailMinShare = 2048, kTailMinBlock = 16;
+    p.n_static = p.n_chunks;
+    p.tail_chunks = 0;
+    p.n_tail = 0;
+    const int64_t max_blocks = std::min<int64_t>(8 * warps, scr.max_ranges - 1 - warps);
+    if (entropy == nullptr && p.n_chunks >= kTailMinShare * warps && max_blocks > 0) {
+        const int64_t tail = p.n_chunks / 16;
+        p.tail_chunks = std::max(kTailMinBlock, (tail + max_blocks - 1) / max_blocks);
+        p.n_tail = (int32_t)((tail + p.tail_chunks - 1) / p.tail_chunks);
+        p.n_static = p.n_chunks - tail;
+    }
+    const int64_t n_ranges = warps + p.n_tail;
     p.npow = npow;
     p.g = g;
     p.n_taus = n_taus;
@@ -187,10 +209,11 @@ ps_status launch_rows(const ps_subtree_batch *b, int sms, const RowsScratch &scr
     p.entropy = entropy;
     p.parts = scr.parts;
     p.counters = scr.counters;
+    p.claim = scr.counters + n_ranges;
     p.status = status;
     const int n_ctas = (int)((warps + ps::kWarpsPerCta - 1) / ps::kWarpsPerCta);
     // the counters must start at zero whatever the scratch held before
-    const size_t zero_bytes = (size_t)((uint8_t *)(p.counters + warps) - (uint8_t *)scr.zero_from);
+    const size_t zero_bytes = (size_t)((uint8_t *)(p.claim + 1) - (uint8_t *)scr.zero_from);
     ps_status st = map_cuda(cudaMemsetAsync(scr.zero_from, 0, zero_bytes, stream));
     if (st != PS_OK) return st;
     return map_cuda(ps::launch_score_rows(p, n_ctas, stream));
@@ -210,7 +233,7 @@ ps_status score_rows_launch(const ps_subtree_batch *b, double *lp0, double *lq,
     if (st != PS_OK) return st;
     uint8_t *ws = (uint8_t *)workspace;
     int32_t *cnt = (int32_t *)(ws + wl.cnt_off);
-    const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxWarps, cnt};
+    const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxRanges, cnt};
     return launch_rows(b, sms, scr, lp0, lq, entropy, status, cuda_stream, npow, g, tau_pow,
                        n_taus, lq_multi);
 }
@@ -397,7 +420,7 @@ ps_status ps_score_walk_subtree(const ps_subtree_batch *b, const ps_tree *t,
     int32_t *cnt = (int32_t *)(ws + wl.cnt_off);
     if (b->n_rows > 0) {
         // one memset clears the chain counters and the row kernel's counters
-        const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxWarps, chain_cnt};
+        const RowsScratch scr{(ps::RowPart *)(ws + wl.parts_off), cnt, ps::kMaxRanges, chain_cnt};
         st = launch_rows(b, sms, scr, lp0, lq, out->entropy, out->status, cuda_stream,
                          integer_power(b->tau), (float)(1.0 / b->tau), nullptr, 0, nullptr);
     } else {
@@ -543,10 +566,10 @@ ps_status ps_validate_subtree(const ps_subtree_batch *b, const ps_tree *t, char 
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int64_t kNoAllocMaxRows = 262144;     // per-row values kept in the array
-constexpr int kNoAllocMaxWarps = 4096;           // split-row partials and counters
+constexpr int kNoAllocMaxRanges = 4096;          // chunk ranges: split-row partials, counters
 constexpr size_t kNoAllocRowBytes = (size_t)kNoAllocMaxRows * 2 * sizeof(double);
-constexpr size_t kNoAllocPartBytes = (size_t)2 * kNoAllocMaxWarps * sizeof(ps::RowPart);
-constexpr size_t kNoAllocCntBytes = (size_t)kNoAllocMaxWarps * sizeof(int32_t);
+constexpr size_t kNoAllocPartBytes = (size_t)2 * kNoAllocMaxRanges * sizeof(ps::RowPart);
+constexpr size_t kNoAllocCntBytes = (size_t)kNoAllocMaxRanges * sizeof(int32_t);
 constexpr size_t kNoAllocBytes = kNoAllocRowBytes + kNoAllocPartBytes + kNoAllocCntBytes;
 }  // namespace
 
@@ -597,7 +620,7 @@ extern "C" ps_status ps_score_subtree_noalloc(const ps_subtree_batch *b, const p
     double *lq = lq_scratch ? (double *)base + kNoAllocMaxRows : out->lq;
     if (b->n_rows > 0) {
         int32_t *cnt = (int32_t *)(base + kNoAllocRowBytes + kNoAllocPartBytes);
-        const RowsScratch scr{(ps::RowPart *)(base + kNoAllocRowBytes), cnt, kNoAllocMaxWarps,
+        const RowsScratch scr{(ps::RowPart *)(base + kNoAllocRowBytes), cnt, kNoAllocMaxRanges,
                               cnt};
         st = launch_rows(b, sms, scr, lp0, lq, out->entropy, out->status, cuda_stream,
                          integer_power(b->tau), (float)(1.0 / b->tau), nullptr, 0, nullptr);

@@ -11,13 +11,16 @@ namespace ps {
 // ---------------------------------------------------------------------------
 // Scoring kernel geometry (K1).  Each warp streams its own contiguous range of
 // row chunks through a private ring of shared-memory stages filled by 1-D bulk
-// copies; see ps_score_rows.cu.
+// copies, then takes tail blocks of the remaining chunks until none is left;
+// see ps_score_rows.cu.
 // ---------------------------------------------------------------------------
 constexpr int kWarpsPerCta = 16;
 constexpr int kStages = 2;
 constexpr int kStageBytes = 4096;
 constexpr int kMaxCtas = 2048;                        // workspace sizing bound
-constexpr int kMaxWarps = kMaxCtas * kWarpsPerCta;
+// chunk ranges (warps' own ranges and tail blocks, plus the claim counter)
+// that a workspace holds split-row partials and counters for
+constexpr int kMaxRanges = kMaxCtas * kWarpsPerCta;
 
 // Partial log-sum-exp state of (part of) a row: with y = l*log2e - R, the
 // sums of 2^y, 2^(g*y) and 2^y * y over the row's elements except the token,
@@ -46,7 +49,11 @@ struct RowsParams {
     int32_t row_bytes;          // V * elem rounded up to 16
     int32_t cpr;                // chunks per row
     int64_t n_chunks;           // n_rows * cpr
-    int32_t n_vwarps;           // warps that own a non-empty chunk range
+    int32_t n_vwarps;           // warps, each owning one static chunk range
+    int64_t n_static;           // the static ranges cover chunks [0, n_static)
+    int64_t tail_chunks;        // chunks per tail block (0 when there are none)
+    int32_t n_tail;             // tail blocks over [n_static, n_chunks)
+    int32_t *claim;             // tail blocks taken so far; zero at launch
     int32_t npow;               // 1/tau when it is 1, 2, 4 or 8; 16 (17): several
                                 // temperatures with 1/tau in {1, 2, 4, 8} ({1, 2, 4}),
                                 // listed in tau_pow; else 0
@@ -57,8 +64,8 @@ struct RowsParams {
     double *lp0;
     double *lq;
     double *entropy;            // optional: entropy of p0 per row
-    RowPart *parts;             // [2 * kMaxWarps]
-    int32_t *counters;          // [kMaxWarps]
+    RowPart *parts;             // [2 * (n_vwarps + n_tail)], two per chunk range
+    int32_t *counters;          // [n_vwarps + n_tail], one per chunk range
     int32_t *status;
 };
 

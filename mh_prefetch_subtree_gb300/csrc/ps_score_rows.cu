@@ -25,19 +25,24 @@
 // Data movement.  The rows are cut into chunks of one stage (the last chunk of
 // a row may be shorter).  The chunk sequence of all rows is split into
 // contiguous ranges, one per warp, so every warp streams about the same number
-// of bytes whatever the row count.  Each warp owns a ring of shared-memory
-// stages that its lane 0 fills with 1-D bulk copies (cp.async.bulk,
-// completion on an mbarrier, L2 evict-first since every byte is read once);
-// the warp consumes a stage, refills it, and moves on.  There is no
+// of bytes whatever the row count.  In the variants without entropy, on large
+// batches, those ranges cover the first 15/16 of the sequence only; the rest
+// is cut into small tail blocks, which the warps that finish their own range
+// first take one at a time (an atomic counter), so that SMs that read a little
+// slower than the others do not decide when the kernel ends.  Each warp owns a ring of
+// shared-memory stages that its lane 0 fills with 1-D bulk copies
+// (cp.async.bulk, completion on an mbarrier, L2 evict-first since every byte
+// is read once); the warp consumes a stage, refills it, and moves on.  There is no
 // block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
 // row's token logit (after saving it) and any padding beyond V with -inf (in
 // the entropy variant with -1e30, which adds nothing either but keeps
 // 2^y y finite on the clamp-free fast path).
 //
-// A row whose chunks all lie in one warp's range is finalised by that warp.
-// A row split across warps leaves one partial per warp in the workspace; the
-// last warp to arrive (atomic counter) merges them in warp order and
-// finalises.  Results are deterministic.
+// A row whose chunks all lie in one range is finalised by the warp that reads
+// that range.  A row split across ranges leaves one partial per range in the
+// workspace; the last warp to arrive (atomic counter) merges them in range
+// order and finalises.  Results are deterministic: they do not depend on
+// which warp read which tail block.
 #include <math.h>
 
 #include "ps_internal.cuh"
@@ -58,6 +63,7 @@ constexpr uint32_t kAbsent = 0x7fc0deadu;           // "token not in this part" 
 constexpr uint32_t kFloorBf16x2 = 0xf14af14au;      // (-1.0009e30, -1.0009e30) as bf16x2
 constexpr float kFloorF32 = -1.0e30f;
 
+// Warp w's chunk range is [range_begin(w), range_begin(w + 1)).
 __device__ __forceinline__ int64_t range_begin(int64_t w, int64_t C, int64_t W) {
     return (w * C) / W;
 }
@@ -69,6 +75,23 @@ __device__ __forceinline__ int64_t warp_of_chunk(int64_t c, int64_t C, int64_t W
     while (w + 1 < W && range_begin(w + 1, C, W) <= c) ++w;
     while (w > 0 && range_begin(w, C, W) > c) --w;
     return w;
+}
+
+// Chunk ranges with tail blocks.  Ranges 0..W-1 (W = n_vwarps) split chunks
+// [0, n_static) as above, one per warp; ranges W..W+n_tail-1 are the tail
+// blocks of tail_chunks chunks each over [n_static, n_chunks), taken at run
+// time by whichever warps finish their own range first.  Every range is
+// non-empty, and tail_range_begin(W + n_tail) = n_chunks.
+__device__ __forceinline__ int64_t tail_range_begin(const RowsParams &p, int64_t r) {
+    const int64_t W = p.n_vwarps;
+    if (r > W) return min(p.n_chunks, p.n_static + (r - W) * p.tail_chunks);
+    return range_begin(r, p.n_static, W);
+}
+
+// The range that holds chunk c.
+__device__ __forceinline__ int64_t tail_range_of_chunk(const RowsParams &p, int64_t c) {
+    if (c >= p.n_static) return p.n_vwarps + (c - p.n_static) / p.tail_chunks;
+    return warp_of_chunk(c, p.n_static, p.n_vwarps);
 }
 
 template <int DT>
@@ -721,20 +744,283 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_rows_kernel(const RowsPar
     pdl_launch_dependents();
 }
 
+// The scoring kernel of the variants without entropy, with tail blocks: each
+// warp reads its own range, then takes tail blocks (a counter in the
+// workspace) until none is left; on batches without tail blocks it reads its
+// own range only.  The entropy variants use score_rows_kernel above, whose
+// body is the same without the range loop: wrapping that body in the loop
+// made the heaviest of them (any other tau, with entropy) 9% slower on GB300,
+// as its code at the 128-register cap was scheduled differently, while they
+// gain little from tail blocks (they are bound by issue rather than by
+// memory).
+template <int DT, int NP, int WARPS, int STAGES, int SB>
+__global__ void __launch_bounds__(WARPS * 32, 1) score_rows_tail_kernel(const RowsParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kWarpsPerCta = WARPS;
+    constexpr int kStages = STAGES;
+    constexpr int kStageBytes = SB;
+    constexpr int kVecPerLane = SB / 16 / 32;
+    static_assert(SB % 512 == 0, "a stage holds a whole number of 16-byte vectors per lane");
+    constexpr int kEsz = Elem<DT>::kSize;
+    constexpr int kElemsPerStage = kStageBytes / kEsz;
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int64_t W = p.n_vwarps;
+    const int64_t vw = (int64_t)blockIdx.x * kWarpsPerCta + wid;
+    if (vw >= W) return;
+    const int32_t cpr = p.cpr;
+    const float g = p.g;
+
+    uint8_t *stage = smem + (size_t)wid * kStages * kStageBytes;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + (size_t)kWarpsPerCta * kStages * kStageBytes) +
+        wid * kStages;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t policy = l2_evict_first_policy();   // logits are read once
+    uint32_t phase = 0;                               // mbarrier parity of each stage
+    int s = 0;                                        // stage of the next chunk
+
+    // the warp's own range, then tail blocks until none is left
+    for (int64_t vr = vw;;) {
+        const int64_t cb = tail_range_begin(p, vr);
+        const int64_t ce = tail_range_begin(p, vr + 1);
+
+        // ---- issue side: next chunk to copy and a lane-parallel cache of row_index
+        int64_t ic = cb;
+        int64_t irow = cb / cpr;
+        int32_t ik = (int32_t)(cb - irow * cpr);
+        int64_t ri_base = -1;
+        int64_t ri_reg = 0;
+        auto src_row_of = [&](int64_t row) -> int64_t {   // warp-collective
+            if (p.row_index == nullptr) return row;
+            if (ri_base < 0 || row >= ri_base + 32 || row < ri_base) {
+                ri_base = row;
+                const int64_t rr = row + lane;
+                ri_reg = rr < p.n_rows ? __ldg(p.row_index + rr) : 0;
+            }
+            int64_t sr = __shfl_sync(0xffffffffu, ri_reg, (int)(row - ri_base));
+            if (sr < 0 || sr >= p.n_logit_rows) sr = 0;   // flagged on the consume side
+            return sr;
+        };
+        auto issue_next = [&](int st) {                   // warp-collective
+            const int64_t srow = src_row_of(irow);
+            if (lane == 0) {
+                const uint32_t off = (uint32_t)ik * kStageBytes;
+                const uint32_t bytes = min((uint32_t)kStageBytes, (uint32_t)p.row_bytes - off);
+                const uint8_t *src = p.logits + srow * p.ld_bytes + off;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars[st], bytes);
+                bulk_g2s(stage + (size_t)st * kStageBytes, src, bytes, &bars[st], policy);
+            }
+            ++ic;
+            if (++ik == cpr) {
+                ik = 0;
+                ++irow;
+            }
+        };
+#pragma unroll
+        for (int j = 0; j < kStages; ++j)
+            if (ic < ce) issue_next(s + j < kStages ? s + j : s + j - kStages);
+
+        // ---- consume side
+        int64_t row = cb / cpr;
+        int32_t k = (int32_t)(cb - row * cpr);
+        int64_t tb = -1;
+        int32_t tok_reg = 0;
+        int64_t rib_reg = 0;
+        int32_t tok = 0;
+        bool bad = false;
+        auto row_start = [&]() {                          // warp-collective
+            if (tb < 0 || row >= tb + 32) {
+                tb = row;
+                const int64_t rr = row + lane;
+                tok_reg = rr < p.n_rows ? __ldg(p.tokens + rr) : 0;
+                rib_reg = (p.row_index != nullptr && rr < p.n_rows) ? __ldg(p.row_index + rr) : 0;
+            }
+            tok = __shfl_sync(0xffffffffu, tok_reg, (int)(row - tb));
+            const int64_t src = __shfl_sync(0xffffffffu, rib_reg, (int)(row - tb));
+            const bool bad_tok = tok < 0 || tok >= p.V;
+            const bool bad_src = p.row_index != nullptr && (src < 0 || src >= p.n_logit_rows);
+            bad = bad_tok || bad_src;
+            if (lane == 0) {
+                if (bad_tok) set_status(p.status, PS_DEV_BAD_TOKEN);
+                if (bad_src) set_status(p.status, PS_DEV_BAD_ROW_INDEX);
+            }
+        };
+        row_start();
+
+        Acc acc = acc_empty();
+        float ltok = __uint_as_float(kAbsent);
+
+        for (int64_t c = cb; c < ce; ++c, s = (s + 1 == kStages) ? 0 : s + 1) {
+            if (!mbar_wait_bounded(&bars[s], (phase >> s) & 1u, kWaitLimitNs)) {
+                if (lane == 0) {
+                    set_status(p.status, PS_DEV_TIMEOUT);
+                    // let this warp's copies in flight land before the warp exits
+                    for (int j = 0; j < kStages; ++j) {
+                        if (c + j < ic) {
+                            const int sj = (s + j) % kStages;
+                            mbar_wait_bounded(&bars[sj], (phase >> sj) & 1u, kDrainLimitNs);
+                        }
+                    }
+                }
+                __syncwarp();
+                return;
+            }
+            phase ^= 1u << s;
+            uint8_t *buf = stage + (size_t)s * kStageBytes;
+            const uint32_t off = (uint32_t)k * kStageBytes;
+            const uint32_t bytes = min((uint32_t)kStageBytes, (uint32_t)p.row_bytes - off);
+            if (lane == 0) {
+                const int64_t e0 = (int64_t)k * kElemsPerStage;
+                const int64_t nel = bytes / kEsz;
+                if (!bad) {
+                    const int64_t o = (int64_t)tok - e0;
+                    if (o >= 0 && o < nel) {
+                        if constexpr (DT == PS_BF16) {
+                            uint16_t *h = reinterpret_cast<uint16_t *>(buf) + o;
+                            ltok = __uint_as_float((uint32_t)*h << 16);
+                            *h = 0xff80u;
+                        } else {
+                            float *f = reinterpret_cast<float *>(buf) + o;
+                            ltok = *f;
+                            *f = -INFINITY;
+                        }
+                    }
+                }
+                if (k == cpr - 1) {
+                    for (int64_t j = (int64_t)p.V - e0; j < nel; ++j) {
+                        if constexpr (DT == PS_BF16)
+                            reinterpret_cast<uint16_t *>(buf)[j] = 0xff80u;
+                        else
+                            reinterpret_cast<float *>(buf)[j] = -INFINITY;
+                    }
+                }
+            }
+            __syncwarp();
+            {
+                const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
+                const int nvec = (int)(bytes >> 4);
+                uint4 q[kVecPerLane];
+                load_vecs<DT, kVecPerLane, false>(v4, nvec, lane, q);
+                float c1, ct[3], cy;
+                sum_vecs<DT, NP, false, kVecPerLane, false>(q, acc.R, g, c1, ct, cy);
+                const bool fast = chunk_peak<NP>(c1, ct) <= kLimit;
+                if (fast) {
+                    add_chunk<NP, false>(acc, c1, ct, cy);
+                } else {
+                    acc = slow_chunk<DT, NP, false, kVecPerLane>(v4, nvec, lane, g, acc);
+                }
+            }
+            __syncwarp();
+            if (ic < ce) issue_next(s);
+
+            const bool row_end = (k == cpr - 1) || (c == ce - 1);
+            if (row_end) {
+                acc = warp_merge<NP, false>(acc, g);
+                const float lt = __shfl_sync(0xffffffffu, ltok, 0);
+                const int64_t rc0 = row * cpr, rc1 = rc0 + cpr;
+                if (rc0 >= cb && rc1 <= ce) {
+                    if (lane == 0) finalize_row<NP, false>(p, row, acc, lt, bad);
+                } else {
+                    const int64_t slot = (row == cb / cpr) ? 2 * vr : 2 * vr + 1;
+                    const int64_t owner = tail_range_of_chunk(p, rc0);
+                    const int64_t lastw = tail_range_of_chunk(p, rc1 - 1);
+                    int last = 0;
+                    if (lane == 0) {
+                        RowPart part;
+                        part.R = acc.R;
+                        part.s1 = acc.s1;
+                        part.st = acc.st[0];
+                        part.ltok = lt;
+                        part.y1 = acc.y1;
+                        part.st1 = acc.st[1];
+                        part.st2 = acc.st[2];
+                        part.pad = 0.f;
+                        p.parts[slot] = part;
+                        __threadfence();
+                        const int old = atomicAdd(p.counters + owner, 1);
+                        last = (old == (int)(lastw - owner));
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last) {
+                        __threadfence();
+                        Acc m = acc_empty();
+                        float ltm = __uint_as_float(kAbsent);
+                        // lanes take the parts in range order, then a fixed butterfly
+                        for (int64_t u = owner + lane; u <= lastw; u += 32) {
+                            const int64_t su =
+                                (row == tail_range_begin(p, u) / cpr) ? 2 * u : 2 * u + 1;
+                            const float4 *pp = reinterpret_cast<const float4 *>(p.parts + su);
+                            const float4 pv = __ldcg(pp);
+                            const float4 pw = __ldcg(pp + 1);
+                            m = merge_part<NP, false>(m, Acc{pv.x, pv.y, {pv.z, pw.y, pw.z}, pw.x},
+                                                    g);
+                            if (__float_as_uint(pv.w) != kAbsent) ltm = pv.w;
+                        }
+                        m = warp_merge<NP, false>(m, g);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const float other = __shfl_xor_sync(0xffffffffu, ltm, o);
+                            if (__float_as_uint(ltm) == kAbsent) ltm = other;
+                        }
+                        if (lane == 0) {
+                            finalize_row<NP, false>(p, row, m, ltm, bad);
+                            p.counters[owner] = 0;
+                        }
+                    }
+                }
+                acc = acc_empty();
+                ltok = __uint_as_float(kAbsent);
+            }
+            if (++k == cpr) {
+                k = 0;
+                ++row;
+                if (c + 1 < ce) row_start();
+            }
+        }
+        // every copy issued for this range has been consumed; take a tail block
+        if (p.n_tail == 0) break;
+        int32_t b = 0;
+        if (lane == 0) b = atomicAdd(p.claim, 1);
+        b = __shfl_sync(0xffffffffu, b, 0);
+        if (b >= p.n_tail) break;
+        vr = W + b;
+    }
+    // the next kernel may be launched once every CTA gets here (as in
+    // score_rows_kernel)
+    pdl_launch_dependents();
+}
+
 template <int WARPS, int STAGES, int SB>
 constexpr size_t smem_bytes_for() {
     return (size_t)WARPS * STAGES * SB + (size_t)WARPS * STAGES * 8;
 }
 
-template <int DT, int NP, bool ENT, bool CF>
-cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
-    auto kern = score_rows_kernel<DT, NP, ENT, kWarpsPerCta, kStages, kStageBytes, CF>;
+template <typename Kernel>
+cudaError_t launch_k(Kernel kern, const RowsParams &p, int n_ctas, cudaStream_t stream) {
     const size_t smem = smem_bytes_for<kWarpsPerCta, kStages, kStageBytes>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<n_ctas, kWarpsPerCta * 32, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+// The entropy variants run score_rows_kernel, the others score_rows_tail_kernel.
+template <int DT, int NP, bool ENT, bool CF>
+cudaError_t launch_t(const RowsParams &p, int n_ctas, cudaStream_t stream) {
+    if constexpr (ENT)
+        return launch_k(score_rows_kernel<DT, NP, ENT, kWarpsPerCta, kStages, kStageBytes, CF>,
+                        p, n_ctas, stream);
+    else
+        return launch_k(score_rows_tail_kernel<DT, NP, kWarpsPerCta, kStages, kStageBytes>, p,
+                        n_ctas, stream);
 }
 
 template <int DT, bool ENT, bool CF>
