@@ -47,8 +47,8 @@ NOMINAL_HBM_GBS = 8000.0            # the roofline the target is stated against
 FALLBACK_HBM_GBS = 6800.0           # used only when MEASURED_PEAKS.json is absent
 # DRAM bytes (read + write) per launch of the scoring kernel on the default
 # workload, from one ncu capture of this kernel code (identified by its hash).
-NCU_TRAFFIC = {"source_sha1": "dcbdb4dba69d17f8e3bc89b486db341345447d20",
-               "bytes_per_launch": 29925169152 + 6791936, "config": 3}
+NCU_TRAFFIC = {"source_sha1": "5cb170908f66cd1a695bef1deab314f034cf2fef",
+               "bytes_per_launch": 29925604608 + 7847680, "config": 3}
 GENERAL_TAU = 0.3                   # a temperature whose 1/tau is not 1, 2, 4 or 8
 
 
