@@ -146,13 +146,22 @@ def check_walk(w, g: dict, o: dict) -> dict:
 
 
 def full_parity(w, threads: int | None = None, rows=None) -> dict:
-    g = run_gpu(w)
-    assert g["status"] == 0, ps.dev_status_names(g["status"])
-    assert g["wstatus"] == 0, ps.dev_status_names(g["wstatus"])
-    o = run_oracle(w, threads=threads, rows=rows)
+    """The round computed twice, with the entropy of p0 and without it (the
+    two kinds of scoring kernel: without entropy, large batches take tail
+    blocks), each compared with one oracle run.  The stats of the run without
+    entropy carry the suffix "_no_entropy"."""
+    o = None
     stats = {}
-    stats.update(check_rows(g, o))
-    stats.update(check_log_accept(w, g, o))
-    stats.update(check_walk(w, g, o))
+    for entropy in (True, False):
+        g = run_gpu(w, entropy=entropy)
+        assert g["status"] == 0, ps.dev_status_names(g["status"])
+        assert g["wstatus"] == 0, ps.dev_status_names(g["wstatus"])
+        if o is None:
+            o = run_oracle(w, threads=threads, rows=rows)
+        s = {}
+        s.update(check_rows(g, o))
+        s.update(check_log_accept(w, g, o))
+        s.update(check_walk(w, g, o))
+        stats.update(s if entropy else {k + "_no_entropy": v for k, v in s.items()})
     stats["eps_certain"] = oracle.eps_certain_fraction(o["log_accept"][~w.layout.is_root()])
     return stats

@@ -41,10 +41,12 @@ def w4():
 
 
 def test_tail_blocks_do_not_depend_on_the_order(w4):
-    # three rounds take the blocks in different orders; the bits stay the same
-    runs = [H.run_gpu(w4) for _ in range(3)]
+    # three rounds of the scoring kernel without entropy (the one with tail
+    # blocks) take the blocks in different orders; the bits stay the same
+    runs = [H.run_gpu(w4, entropy=False) for _ in range(3)]
     assert runs[0]["status"] == 0 and runs[0]["wstatus"] == 0
-    for k in ("lp0", "lq", "entropy", "log_accept", "state_seg", "path"):
+    assert runs[0].get("entropy") is None
+    for k in ("lp0", "lq", "log_accept", "state_seg", "path"):
         for r in runs[1:]:
             assert np.array_equal(runs[0][k], r[k], equal_nan=True), k
 
