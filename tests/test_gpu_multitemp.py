@@ -195,3 +195,30 @@ def test_multi_temperature_on_masked_rows_with_and_without_the_hint(V, dtype):
         assert status == 0
         for k, t in enumerate(TABLE6_TAUS):
             _check((lp0, lq[k], ent), _oracle(x, dtype, V, tok, t), f"flags={flags} tau={t}")
+
+
+def test_multi_temperature_with_tail_blocks_at_full_size():
+    # configuration 4 (45,820 rows of 128 chunks) is large enough for tail
+    # blocks in the variant without entropy; every row that reaches into the
+    # last 1/16 of the chunks (the tail blocks) and 2,000 of the others are
+    # compared with the oracle at each temperature
+    from synth import make_workload
+    w = make_workload(4, device=DEV)
+    warps = torch.cuda.get_device_properties(0).multi_processor_count * 16
+    assert w.n_rows * 128 >= 2048 * warps, "the batch is too small to have tail blocks"
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=w.tau, max_steps=w.max_steps)
+    lp0, lq, ent, status = _run_multi(d, TABLE6_TAUS, entropy=False)
+    assert status == 0, ps.dev_status_names(status)
+    assert ent is None
+    n = w.n_rows
+    tail0 = n - n // 16 - 1
+    rng = np.random.default_rng(5)
+    sel = np.unique(np.concatenate([np.arange(tail0, n), rng.choice(tail0, 2000, replace=False)]))
+    idx = torch.from_numpy(sel).to(DEV)
+    xs, ts = w.logits[idx], w.tokens[idx]
+    for k, t in enumerate(TABLE6_TAUS):
+        o = _oracle(xs, "bf16", w.V, ts, t)
+        _check((lp0[sel], lq[k][sel], None), (o[0], o[1], None), f"tau={t}")
+    del d, w
+    torch.cuda.empty_cache()
