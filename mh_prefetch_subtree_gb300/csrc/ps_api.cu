@@ -186,7 +186,7 @@ ps_status launch_rows(const ps_subtree_batch *b, int sms, const RowsScratch &scr
     // slow SM does not set the end.  On smaller batches a block would take
     // about as long as the spread between SMs, and claiming it and refilling
     // the ring cost more than it saves.  The entropy variants have no tail
-    // blocks (the kernel's kTail).
+    // blocks: they run score_rows_kernel, which reads its own range only.
     constexpr int64_t kTailMinShare = 2048, kTailMinBlock = 16;
     p.n_static = p.n_chunks;
     p.tail_chunks = 0;
