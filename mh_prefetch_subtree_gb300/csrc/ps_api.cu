@@ -69,6 +69,12 @@ ps_status device_of(const void *ptr, int *sms) {
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (major * 10 + minor != 103) return PS_ERR_UNSUPPORTED;   // built for sm_103a only
+        // the scoring kernel's rings need this much shared memory per CTA
+        int smem = 0;
+        if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            (size_t)smem < ps::score_rows_smem_bytes())
+            return PS_ERR_UNSUPPORTED;
         cache[dev] = n;
     }
     *sms = cache[dev];
