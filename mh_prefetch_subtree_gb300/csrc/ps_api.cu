@@ -121,7 +121,7 @@ ps_status check_batch_host(const ps_subtree_batch *b, bool need_data = true) {
 
 extern "C" {
 
-const char *ps_version(void) { return "libps 0.3.0 (sm_103a)"; }
+const char *ps_version(void) { return "libps 0.4.0 (sm_103a)"; }
 
 const char *ps_status_string(ps_status s) {
     switch (s) {
