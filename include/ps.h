@@ -190,8 +190,9 @@ typedef struct {
  * Bytes of device workspace the scoring calls need for this batch (depends
  * only on n_rows and n_chains).  The workspace is scratch: per-row results
  * when lp0/lq are not requested, partial sums of rows that are split across
- * warps, their arrival counters, and one arrival counter per chain for
- * ps_score_walk_subtree.  Returns 0 if batch is NULL.
+ * the scoring kernel's chunk ranges, their arrival counters, the counter of
+ * the tail blocks that warps take at run time, and one arrival counter per
+ * chain for ps_score_walk_subtree.  Returns 0 if batch is NULL.
  */
 size_t ps_score_workspace_bytes(const ps_subtree_batch *batch);
 
