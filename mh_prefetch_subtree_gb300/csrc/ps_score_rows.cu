@@ -28,15 +28,15 @@
 // of bytes whatever the row count.  In the variants without entropy, on large
 // batches, those ranges cover the first 15/16 of the sequence only; the rest
 // is cut into small tail blocks, which the warps that finish their own range
-// first take one at a time (an atomic counter), so that SMs that read a little
-// slower than the others do not decide when the kernel ends.  Each warp owns a ring of
-// shared-memory stages that its lane 0 fills with 1-D bulk copies
-// (cp.async.bulk, completion on an mbarrier, L2 evict-first since every byte
-// is read once); the warp consumes a stage, refills it, and moves on.  There is no
-// block-wide synchronisation.  Before a stage is read, lane 0 overwrites the
-// row's token logit (after saving it) and any padding beyond V with -inf (in
-// the entropy variant with -1e30, which adds nothing either but keeps
-// 2^y y finite on the clamp-free fast path).
+// first take one at a time (an atomic counter), so that SMs that read a
+// little slower than the others do not decide when the kernel ends.  Each
+// warp owns a ring of shared-memory stages that its lane 0 fills with 1-D bulk
+// copies (cp.async.bulk, completion on an mbarrier, L2 evict-first since every
+// byte is read once); the warp consumes a stage, refills it, and moves on.
+// There is no block-wide synchronisation.  Before a stage is read, lane 0
+// overwrites the row's token logit (after saving it) and any padding beyond V
+// with -inf (in the entropy variant with -1e30, which adds nothing either but
+// keeps 2^y y finite on the clamp-free fast path).
 //
 // A row whose chunks all lie in one range is finalised by the warp that reads
 // that range.  A row split across ranges leaves one partial per range in the
