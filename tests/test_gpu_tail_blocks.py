@@ -6,8 +6,9 @@ first take at run time.  A row that runs through several ranges (a warp's
 range and tail blocks, or several tail blocks) is merged from one partial per
 range in range order, so the per-row values of PreSTO eq. (6) (log p0 and
 log q_tau of each token, Appendix B.1) must not depend on which warp took
-which block.  The full-size parity tests (configurations 3, 4 and the sweep
-points, which all have tail blocks) compare every row with the oracle; these
+which block.  Tail blocks are taken by the scoring kernel without entropy:
+the full-size parity tests compare every row of its runs with the oracle
+(configurations 3, 4 and the sweep points all have tail blocks there); these
 tests check the order independence and the no-allocation entry point, whose
 smaller static array gives it fewer, larger blocks.
 """
