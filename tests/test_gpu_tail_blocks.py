@@ -74,3 +74,23 @@ def test_tail_blocks_in_the_static_array_of_the_no_alloc_entry_point(w4):
     req = ~w.layout.is_root()
     la, lb = t["log_accept"].cpu().numpy()[req], ref.t["log_accept"].cpu().numpy()[req]
     assert np.all(np.abs(la - lb) <= H.LA_ATOL)
+
+
+def test_tail_blocks_with_float32_rows_match_the_oracle():
+    # float32 rows of V = 151,936 (149 chunks, the last one ragged), 43,663 rows
+    # (26.5 GB): every row of both scoring kernels against the oracle
+    from synth.trees import assemble_layout, bfs_tree
+    from synth.workload import Workload, draw_tokens, gen_logits
+    rng = np.random.default_rng(74)
+    lay = assemble_layout([bfs_tree(rng, 256, 8) for _ in range(30)])
+    warps = torch.cuda.get_device_properties(0).multi_processor_count * 16
+    assert lay.n_rows * 149 >= 2048 * warps, "the batch is too small to have tail blocks"
+    x = gen_logits("boosted", dict(sigma=3.0, margin_mean=4.0), lay.n_rows, 151936, "f32",
+                   seed=75, device=DEV)
+    tok = draw_tokens(x, 0.25, seed=76)
+    w = Workload(name="f32 tail blocks", layout=lay, V=151936, dtype="f32", alpha=4.0, tau=0.25,
+                 logits=x, tokens=tok, u=1.0 - rng.random(lay.n_seg), max_steps=100)
+    s = H.full_parity(w)
+    assert s["lp0_max_rel_no_entropy"] <= H.TOK_RTOL
+    del w, x, tok
+    torch.cuda.empty_cache()
