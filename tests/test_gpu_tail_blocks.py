@@ -94,3 +94,28 @@ def test_tail_blocks_with_float32_rows_match_the_oracle():
     assert s["lp0_max_rel_no_entropy"] <= H.TOK_RTOL
     del w, x, tok
     torch.cuda.empty_cache()
+
+
+def test_tail_blocks_at_a_general_temperature(w4):
+    # tau = 0.3 (1/tau not a power of two: a second exponential per logit), no
+    # entropy: every row that reaches into the tail region and 2,000 others
+    # against the oracle
+    import oracle
+    from oracle.hostcopy import bf16_bits
+    w = w4
+    d = ps.DeviceSubtree.create(layout=w.layout, u=w.u, logits=w.logits, tokens=w.tokens,
+                                V=w.V, alpha=w.alpha, tau=0.3, max_steps=w.max_steps)
+    d.score_rows()
+    torch.cuda.synchronize()
+    assert int(d.t["status"].item()) == 0, ps.dev_status_names(int(d.t["status"].item()))
+    n = w.n_rows
+    tail0 = n - n // 16 - 1
+    rng = np.random.default_rng(6)
+    sel = np.unique(np.concatenate([np.arange(tail0, n), rng.choice(tail0, 2000, replace=False)]))
+    idx = torch.from_numpy(sel).to(DEV)
+    o = oracle.row_logprobs(bf16_bits(w.logits[idx]), "bf16", w.V, w.tokens[idx].cpu().numpy(),
+                            0.3, entropy=False)
+    g = {"lp0": d.t["lp0"].cpu().numpy()[sel], "lq": d.t["lq"].cpu().numpy()[sel]}
+    H.check_rows(g, {"lp0": o[0], "lq": o[1]})
+    del d
+    torch.cuda.empty_cache()
