@@ -762,13 +762,13 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (a read+write copy; a read-only "
                                     "stream can exceed it)",
-                     "kernel": "score_rows_kernel", "kernel_ms": k1_avg,
+                     "kernel": "score_rows_tail_kernel", "kernel_ms": k1_avg,
                      "algorithmic_bytes": alg_bytes_k1,
                      "frac_of_8TBps": achieved / NOMINAL_HBM_GBS},
         "logits_GBps": logits_bytes / (k1_avg / 1e3) / 1e9,
         "rows_per_s": whole_job_rate(rows, ws, args.steps, total_ms),
         "gpu_launches": 2 * args.steps,
-        "kernel_launches_per_step": {"score_rows_kernel": 1,
+        "kernel_launches_per_step": {"score_rows_tail_kernel (scoring)": 1,
                                      "assemble_kernel (suffix sums, log A and the walk)": 1},
         # what the suffix sums, log A and the walk add to a step after scoring
         "after_scoring_us": tail["median_us"],
